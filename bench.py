@@ -1,0 +1,426 @@
+"""Benchmark of the sparse MoE layer forward on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one full layer forward (router, capacity + dispatch, expert FFNs,
+combine) over one batch of the workload, inputs resident in HBM. The step is
+issued as the four stage calls of the C ABI (moe_route, moe_dispatch,
+moe_expert_ffn, moe_combine: exactly the launches moe_forward makes) with CUDA
+events between them on the launching stream, so the per-stage times come from
+the timed region itself. L2 is flushed (a 512 MiB write) between timed steps,
+outside the events. ``e2e`` times moe_forward with the batch copied from pinned
+host memory and the output copied back inside each step.
+
+Multi-GPU: replicas only (capacity couples every token of a batch, so a batch
+is not split); every rank runs its own batch and value = all tokens / the
+slowest rank's time. Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_mixture_experts_66_b300 import moe  # noqa: E402
+from sparse_mixture_experts_66_b300.workload import HEADLINE, WORKLOADS, as_f32_numpy, draw  # noqa: E402
+
+METRIC = "MoE-layer fwd tokens/s on 1 B300; % of bf16 tensor / HBM roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+KERNELS_PER_STEP = 7  # router, capacity select, capacity assign, permute, GEMM1, GEMM2, combine
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (barrier + max over ranks only; no data-path collective)
+# ---------------------------------------------------------------------------
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    if world == 1:
+        return value
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(units_per_rank: float, seconds_per_rank: float, world: int, device) -> tuple:
+    """Whole-job throughput of replicas: all ranks' units over the slowest rank's time."""
+    slowest = max_over_ranks(seconds_per_rank, world, device)
+    return units_per_rank * world / slowest, slowest
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.file,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+class Stages:
+    """The four stage calls of one forward, on workspace buffers."""
+
+    def __init__(self, cfg, dev, ws):
+        self.cfg, self.dev, self.ws = cfg, dev, ws
+        self.v = ws.views()
+        self.y = torch.empty_like(dev["x"])
+
+    def route(self, s):
+        d, v = self.dev, self.v
+        moe.moe_route(self.cfg, d["x"], d["w_g"], d["router_bias"], v["topk_idx"], v["gate"], v["score"], self.ws.buf,
+                      s)
+
+    def dispatch(self, s):
+        d, v = self.dev, self.v
+        moe.moe_dispatch(self.cfg, d["x"], v["topk_idx"], v["gate"], v["score"], v["counts_raw"], v["counts_kept"],
+                         v["offsets"], v["row_of"], v["row_token"], v["row_gate"], v["x_perm"], self.ws.buf, s)
+
+    def ffn(self, s):
+        d, v = self.dev, self.v
+        moe.moe_expert_ffn(self.cfg, v["x_perm"], v["offsets"], d["w1"], d["b1"], d["w2"], d["b2"], v["row_gate"],
+                           v["h"], v["y_perm"], self.ws.buf, s)
+
+    def combine(self, s):
+        v = self.v
+        moe.moe_combine(self.cfg, v["y_perm"], v["row_of"], v["gate"], self.dev["x"], self.y, self.ws.buf, s)
+
+    def all(self, s):
+        self.route(s)
+        self.dispatch(s)
+        self.ffn(s)
+        self.combine(s)
+
+
+def algorithmic(w, counts_kept):
+    """Algorithmic FLOPs and bytes of one forward (kept rows only; padding and
+    intermediates excluded)."""
+    s = 2 if w.dtype == "bf16" else 4
+    R = int(np.sum(counts_kept))
+    A = int(np.sum(np.asarray(counts_kept) > 0))
+    flops_router = 2.0 * w.T * w.d * w.N
+    flops_ffn = 4.0 * R * w.d * w.d_ff
+    bytes_total = 2.0 * w.T * w.d * s + w.N * w.d * s + A * (2.0 * w.d * w.d_ff + w.d_ff + w.d) * s
+    bytes_ffn_weights = A * (2.0 * w.d * w.d_ff + w.d_ff + w.d) * s
+    return dict(R=R, A=A, flops=flops_router + flops_ffn, flops_ffn=flops_ffn, bytes=bytes_total,
+                bytes_ffn_weights=bytes_ffn_weights)
+
+
+def run_ours(args, world, rank, local):
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    inp = draw(w)
+    dev = {k: (None if v is None else v.to(device)) for k, v in inp.items()}
+    cfg = moe.config_of(w)
+    ws = moe.Workspace(cfg, device=device)
+    st = Stages(cfg, dev, ws)
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)
+
+    for _ in range(max(args.warmup, 3)):
+        st.all(stream)
+    torch.cuda.synchronize(device)
+    ws.status(stream)
+    counts_kept = st.v["counts_kept"].cpu().numpy()
+    alg = algorithmic(w, counts_kept)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize(device)
+    t_wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()  # evict L2 between steps, outside the step's events
+        e = ev[i]
+        e[0].record(stream)
+        st.route(stream)
+        e[1].record(stream)
+        st.dispatch(stream)
+        e[2].record(stream)
+        st.ffn(stream)
+        e[3].record(stream)
+        st.combine(stream)
+        e[4].record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    t_wall = time.perf_counter() - t_wall0
+    clk = clocks.stop()
+    ws.status(stream)
+
+    step_ms = [e[0].elapsed_time(e[4]) for e in ev]
+    stage_ms = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev)
+                for j, n in enumerate(["route", "dispatch", "expert_ffn", "combine"])}
+    ms = statistics.mean(step_ms)
+    value, slowest_s = aggregate_throughput(w.T / (ms * 1e-3), ms * 1e-3, world, device)
+    ms_max = slowest_s * 1e3
+
+    # end to end through moe_forward with host buffers
+    x_host = inp["x"].pin_memory()
+    y_host = torch.empty_like(x_host).pin_memory()
+    x_dev = torch.empty_like(dev["x"])
+    y_dev = torch.empty_like(dev["x"])
+    for _ in range(3):
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.moe_forward(cfg, x_dev, dev["w_g"], dev["router_bias"], dev["w1"], dev["b1"], dev["w2"], dev["b2"],
+                        y_dev, ws.buf, stream)
+        y_host.copy_(y_dev, non_blocking=True)
+    torch.cuda.synchronize(device)
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    barrier(world)
+    for i in range(K):
+        flush.zero_()
+        e2e_ev[i][0].record(stream)
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.moe_forward(cfg, x_dev, dev["w_g"], dev["router_bias"], dev["w1"], dev["b1"], dev["w2"], dev["b2"],
+                        y_dev, ws.buf, stream)
+        y_host.copy_(y_dev, non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    ws.status(stream)
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)
+    e2e_value, _ = aggregate_throughput(w.T / (e2e_ms * 1e-3), e2e_ms * 1e-3, world, device)
+    es = 2 if w.dtype == "bf16" else 4
+
+    peaks, peak_src = load_peaks()
+    t_ffn = stage_ms["expert_ffn"] * 1e-3
+    t_tensor = alg["flops"] / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = alg["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    if t_tensor >= t_hbm:
+        achieved = alg["flops_ffn"] / t_ffn / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"],
+                "frac_of_sustained": achieved / peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]),
+                "peak_source": f"{peak_src} bf16 dense (burst)"}
+    else:
+        achieved = alg["bytes_ffn_weights"] / t_ffn / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "frac_of_8TBs": achieved / 8000.0,
+                "peak_source": f"{peak_src} HBM copy"}
+    roof["traffic"] = None
+    roof["kernel"] = "expert FFN: grouped GEMM1 (+b1, GELU) and GEMM2 (+b2, gate scale), 2 launches per step"
+    roof["algorithmic_per_step"] = alg["flops_ffn"] if roof["bound"] == "tensor" else alg["bytes_ffn_weights"]
+
+    step_flops = alg["flops"] / (ms * 1e-3) / 1e12
+    step_gbs = alg["bytes"] / (ms * 1e-3) / 1e9
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic: seeded normal draws (torch CPU generator, seed 0), fan-in scaled weights",
+        "config": {"workload": w.name, "T": w.T, "d": w.d, "N": w.N, "k": w.k, "d_ff": w.d_ff,
+                   "capacity_factor": None if math.isinf(w.capacity_factor) else w.capacity_factor,
+                   "router_bias": w.router_bias, "capacity": ws.layout.capacity, "kept_rows": alg["R"],
+                   "active_experts": alg["A"], "parallelism": f"replicas{world}",
+                   "l2": "flushed between timed steps (512 MiB write outside the step events)"},
+        "roofline": roof,
+        "step": {"tflops": step_flops, "gbs": step_gbs,
+                 "frac_tensor_roofline": (alg["flops"] / (peaks["bf16_tflops"] * 1e12)) / (ms * 1e-3),
+                 "frac_hbm_roofline": (alg["bytes"] / (peaks["hbm_gbs"] * 1e9)) / (ms * 1e-3),
+                 "stages_ms": stage_ms, "ms_min": min(step_ms), "ms_median": statistics.median(step_ms),
+                 "wall_s": t_wall},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": w.T * w.d * es,
+                "d2h_bytes_per_step": w.T * w.d * es, "ms_per_step": e2e_ms},
+        "gpu_launches": KERNELS_PER_STEP * K,
+        "clocks": clk,
+    }
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, inp, budget_s=args.cpu_budget)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle as a baseline
+# ---------------------------------------------------------------------------
+def _oracle_inputs(inp):
+    return tuple(as_f32_numpy(inp[n]) for n in ("x", "w_g", "w1", "b1", "w2", "b2")), as_f32_numpy(inp["router_bias"])
+
+
+def _oracle_step(orc, w, arrays, rb, n_tok):
+    """Route and apply capacity to the whole batch, run the FFNs and combine for
+    the first n_tok tokens; returns seconds."""
+    t0 = time.perf_counter()
+    orc.forward(*arrays, k=w.k, cf=w.capacity_factor, router_bias=rb, sel=np.arange(n_tok, dtype=np.int64))
+    return time.perf_counter() - t0
+
+
+def _oracle_costs(orc, w, arrays, rb, budget_s):
+    """Fixed cost (routing + capacity of the batch) and per-token cost (expert
+    FFNs + combine) of the oracle, and the sample size that fits the budget."""
+    fixed = _oracle_step(orc, w, arrays, rb, 0)
+    probe = min(w.T, 16)
+    t = _oracle_step(orc, w, arrays, rb, probe)
+    per_tok = max(t - fixed, 1e-9) / probe
+    n = int(max(probe, min(w.T, (budget_s - fixed) / per_tok)))
+    return fixed, per_tok, n
+
+
+def cpu_baseline(w, inp, budget_s=15.0):
+    import oracle
+
+    orc = oracle.load()
+    arrays, rb = _oracle_inputs(inp)
+    fixed, per_tok, n = _oracle_costs(orc, w, arrays, rb, budget_s)
+    t = _oracle_step(orc, w, arrays, rb, n)
+    per_tok = max(t - fixed, 1e-9) / n
+    est = fixed + per_tok * w.T
+    cores = len(os.sched_getaffinity(0))
+    return {"value": w.T / est, "unit": "tokens/s", "cores": int(os.environ.get("OMP_NUM_THREADS", cores)),
+            "kind": "oracle",
+            "sample": f"routing+capacity over all {w.T} tokens ({fixed:.2f} s) and expert FFNs+combine for "
+                      f"{n} of {w.T} tokens ({t - fixed:.2f} s); tokens/s extrapolated to the whole batch",
+            "seconds": t}
+
+
+def run_reference(args, world, rank):
+    """The oracle timed on the host cores as the reference arm."""
+    w = WORKLOADS[args.workload]
+    inp = draw(w)
+    import oracle
+
+    orc = oracle.load()
+    arrays, rb = _oracle_inputs(inp)
+    steps = args.steps + args.warmup
+    fixed, per_tok, _ = _oracle_costs(orc, w, arrays, rb, 1e9)
+    per_step_budget = max(args.ref_budget / steps, fixed + per_tok)
+    n = int(max(1, min(w.T, (per_step_budget - fixed) / per_tok)))
+    for _ in range(args.warmup):
+        _oracle_step(orc, w, arrays, rb, n)
+    ts = [_oracle_step(orc, w, arrays, rb, n) for _ in range(args.steps)]
+    t = statistics.mean(ts)
+    est = fixed + max(t - fixed, 1e-9) / n * w.T
+    value = w.T / est
+    cores = int(os.environ.get("OMP_NUM_THREADS", len(os.sched_getaffinity(0))))
+    sample = (f"each step: routing+capacity over all {w.T} tokens and expert FFNs+combine for {n} of {w.T} "
+              f"tokens (fp64 CPU oracle); tokens/s extrapolated to the whole batch")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": est * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (same draws as ours)",
+            "config": {"workload": w.name, "T": w.T, "d": w.d, "N": w.N, "k": w.k, "d_ff": w.d_ff,
+                       "parallelism": "host cores"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ref-budget", type=float, default=90.0)
+    args = ap.parse_args()
+    world, rank, local = dist_info()
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, world, rank)), flush=True)
+        return
+    init_dist(world, "nccl")
+    out = run_ours(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

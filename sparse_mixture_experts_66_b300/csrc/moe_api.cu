@@ -1,0 +1,290 @@
+// The C ABI declared in include/moe.h: argument checks, workspace layout and
+// the stream-ordered sequence of kernel launches. No allocation, no host
+// synchronisation (except moe_get_device_status, which exists to wait).
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "moe_internal.cuh"
+
+using namespace moe;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+moe_status fail(moe_status st, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+moe_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(MOE_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+int64_t capacity_of(int64_t T, int32_t N, int32_t k, double cf) {
+  if (!(cf > 0.0) || isinf(cf)) return T;
+  const double c = ceil(cf * (double)(T * (int64_t)k) / (double)N);
+  if (!(c < (double)T)) return T;
+  return (int64_t)c;
+}
+
+moe_status check_config(const moe_config *cfg, Dims *D) {
+  if (!cfg) return fail(MOE_ERR_INVALID_ARG, "config is NULL");
+  if (cfg->T < 1) return fail(MOE_ERR_INVALID_ARG, "T must be >= 1 (got %lld)", (long long)cfg->T);
+  if (cfg->N < 1 || cfg->N > 256) return fail(MOE_ERR_INVALID_ARG, "N must be in [1, 256] (got %d)", cfg->N);
+  if (cfg->k < 1 || cfg->k > cfg->N || cfg->k > 8)
+    return fail(MOE_ERR_INVALID_ARG, "k must be in [1, min(N, 8)] (got %d)", cfg->k);
+  if (cfg->T * (int64_t)cfg->k >= ((int64_t)1 << 31)) return fail(MOE_ERR_INVALID_ARG, "T*k must be < 2^31");
+  if (cfg->dtype != MOE_DT_F32 && cfg->dtype != MOE_DT_BF16)
+    return fail(MOE_ERR_INVALID_ARG, "dtype must be MOE_DT_F32 or MOE_DT_BF16");
+  const int64_t mult = cfg->dtype == MOE_DT_BF16 ? 8 : 4;
+  if (cfg->d < 8 || cfg->d % mult || cfg->d_ff < 8 || cfg->d_ff % mult)
+    return fail(MOE_ERR_INVALID_ARG, "d and d_ff must be >= 8 and multiples of %lld (got d=%lld d_ff=%lld)",
+                (long long)mult, (long long)cfg->d, (long long)cfg->d_ff);
+  if (cfg->flags & ~(uint32_t)(MOE_FLAG_RENORM_SURVIVORS | MOE_FLAG_IDENTITY_FALLBACK))
+    return fail(MOE_ERR_INVALID_ARG, "unknown flag bits 0x%x", cfg->flags);
+  if (isnan(cfg->capacity_factor)) return fail(MOE_ERR_INVALID_ARG, "capacity_factor is NaN");
+  D->T = cfg->T;
+  D->d = cfg->d;
+  D->d_ff = cfg->d_ff;
+  D->N = cfg->N;
+  D->k = cfg->k;
+  D->C = capacity_of(cfg->T, cfg->N, cfg->k, cfg->capacity_factor);
+  int64_t S = cfg->T * (int64_t)cfg->k;
+  if ((int64_t)cfg->N * D->C < S) S = (int64_t)cfg->N * D->C;
+  D->R_max = (S + (int64_t)(kRowAlign - 1) * cfg->N) / kRowAlign * kRowAlign;
+  if (D->R_max >= ((int64_t)1 << 31)) return fail(MOE_ERR_INVALID_ARG, "too many permuted rows");
+  D->dt = cfg->dtype;
+  D->flags = cfg->flags;
+  return MOE_OK;
+}
+
+void make_layout(const Dims &D, moe_workspace_layout *L) {
+  const size_t es = D.dt == MOE_DT_BF16 ? 2 : 4;
+  const size_t Tk = (size_t)(D.T * D.k), R = (size_t)D.R_max, N = (size_t)D.N;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  L->status = take(64);
+  L->topk_idx = take(Tk * 4);
+  L->gate = take(Tk * 4);
+  L->score = take(Tk * 4);
+  L->counts_raw = take(N * 4);
+  L->counts_kept = take(N * 4);
+  L->offsets = take((N + 1) * 4);
+  L->sel_thr = take(N * 4);
+  L->sel_eq = take(N * 4);
+  L->row_of = take(Tk * 4);
+  L->row_token = take(R * 4);
+  L->row_gate = take(R * 4);
+  L->x_perm = take(R * (size_t)D.d * es);
+  L->h = take(R * (size_t)D.d_ff * es);
+  L->y_perm = take(R * (size_t)D.d * 4);
+  L->total = off;
+  L->rows = D.R_max;
+  L->capacity = D.C;
+}
+
+#define AT(ws, off, T) reinterpret_cast<T>(static_cast<char *>(ws) + (off))
+
+moe_status check_ptrs(std::initializer_list<const void *> ps, const char *what) {
+  for (const void *p : ps) {
+    if (!p) return fail(MOE_ERR_INVALID_ARG, "%s: a required pointer is NULL", what);
+    if (!aligned16(p)) return fail(MOE_ERR_INVALID_ARG, "%s: pointer %p is not 16-byte aligned", what, p);
+  }
+  return MOE_OK;
+}
+
+moe_status check_opt(const void *p, const char *what) {
+  if (p && !aligned16(p)) return fail(MOE_ERR_INVALID_ARG, "%s: pointer %p is not 16-byte aligned", what, p);
+  return MOE_OK;
+}
+
+#define TRY(expr)                          \
+  do {                                     \
+    moe_status _st = (expr);               \
+    if (_st != MOE_OK) return _st;         \
+  } while (0)
+
+moe_status do_route(const Dims &D, const moe_workspace_layout &L, const void *x, const void *w_g,
+                    const float *router_bias, int32_t *topk_idx, float *gate, float *score, void *ws,
+                    cudaStream_t s) {
+  cudaError_t e = launch_router(D, x, w_g, router_bias, topk_idx, gate, score, AT(ws, L.status, int32_t *), s);
+  if (e != cudaSuccess) return cuda_fail(e, "router launch");
+  return MOE_OK;
+}
+
+moe_status do_dispatch(const Dims &D, const moe_workspace_layout &L, const void *x, const int32_t *topk_idx,
+                       const float *gate, const float *score, int32_t *counts_raw, int32_t *counts_kept,
+                       int32_t *offsets, int32_t *row_of, int32_t *row_token, float *row_gate, void *x_perm,
+                       void *ws, cudaStream_t s) {
+  int32_t *status = AT(ws, L.status, int32_t *);
+  cudaError_t e = launch_capacity(D, topk_idx, gate, score, counts_raw, counts_kept, offsets,
+                                  AT(ws, L.sel_thr, uint32_t *), AT(ws, L.sel_eq, int32_t *), row_of, row_token,
+                                  row_gate, status, s);
+  if (e != cudaSuccess) return cuda_fail(e, "capacity launch");
+  e = launch_permute(D, x, offsets, row_token, x_perm, status, s);
+  if (e != cudaSuccess) return cuda_fail(e, "permute launch");
+  return MOE_OK;
+}
+
+moe_status do_ffn(const Dims &D, const moe_workspace_layout &L, const void *x_perm, const int32_t *offsets,
+                  const void *w1, const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
+                  float *y_perm, void *ws, cudaStream_t s) {
+  int32_t *status = AT(ws, L.status, int32_t *);
+  cudaError_t e = launch_ffn_simt(D, 1, x_perm, D.d, w1, b1, D.d_ff, nullptr, offsets, h, status, s);
+  if (e != cudaSuccess) return cuda_fail(e, "expert GEMM1 launch");
+  e = launch_ffn_simt(D, 2, h, D.d_ff, w2, b2, D.d, row_gate, offsets, y_perm, status, s);
+  if (e != cudaSuccess) return cuda_fail(e, "expert GEMM2 launch");
+  return MOE_OK;
+}
+
+moe_status do_combine(const Dims &D, const moe_workspace_layout &L, const float *y_perm, const int32_t *row_of,
+                      const float *gate, const void *x, void *y, void *ws, cudaStream_t s) {
+  cudaError_t e = launch_combine(D, y_perm, row_of, gate, x, y, AT(ws, L.status, int32_t *), s);
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_version(void) { return "sparse-moe-b300 0.1 (sm_103a)"; }
+
+const char *moe_last_error(void) { return g_err; }
+
+int64_t moe_capacity(const moe_config *cfg) {
+  Dims D;
+  if (check_config(cfg, &D) != MOE_OK) return -1;
+  return D.C;
+}
+
+moe_status moe_get_workspace_layout(const moe_config *cfg, moe_workspace_layout *out) {
+  Dims D;
+  TRY(check_config(cfg, &D));
+  if (!out) return fail(MOE_ERR_INVALID_ARG, "layout output is NULL");
+  make_layout(D, out);
+  return MOE_OK;
+}
+
+size_t moe_workspace_bytes(const moe_config *cfg) {
+  Dims D;
+  if (check_config(cfg, &D) != MOE_OK) return 0;
+  moe_workspace_layout L;
+  make_layout(D, &L);
+  return L.total;
+}
+
+moe_status moe_workspace_init(const moe_config *cfg, void *ws, moe_stream_t stream) {
+  Dims D;
+  TRY(check_config(cfg, &D));
+  TRY(check_ptrs({ws}, "moe_workspace_init"));
+  cudaError_t e = cudaMemsetAsync(ws, 0, 64, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace init");
+  return MOE_OK;
+}
+
+moe_status moe_get_device_status(void *ws, moe_stream_t stream) {
+  if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
+  int32_t h[4] = {0, 0, 0, 0};
+  cudaError_t e = cudaMemcpyAsync(h, ws, sizeof(h), cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status");
+  if (h[0] == 0) return MOE_OK;
+  if (h[0] == MOE_ERR_TIMEOUT || h[0] == MOE_ERR_BOUNDS)
+    return fail((moe_status)h[0], "device error %d recorded by kernel %d (detail %d)", h[0], h[1], h[2]);
+  return fail(MOE_ERR_CUDA, "unknown device status %d (kernel %d, detail %d)", h[0], h[1], h[2]);
+}
+
+moe_status moe_route(const moe_config *cfg, const void *x, const void *w_g, const float *router_bias,
+                     int32_t *topk_idx, float *gate, float *score, void *ws, moe_stream_t stream) {
+  Dims D;
+  TRY(check_config(cfg, &D));
+  TRY(check_ptrs({x, w_g, topk_idx, gate, score, ws}, "moe_route"));
+  TRY(check_opt(router_bias, "moe_route router_bias"));
+  moe_workspace_layout L;
+  make_layout(D, &L);
+  return do_route(D, L, x, w_g, router_bias, topk_idx, gate, score, ws, (cudaStream_t)stream);
+}
+
+moe_status moe_dispatch(const moe_config *cfg, const void *x, const int32_t *topk_idx, const float *gate,
+                        const float *score, int32_t *counts_raw, int32_t *counts_kept, int32_t *offsets,
+                        int32_t *row_of, int32_t *row_token, float *row_gate, void *x_perm, void *ws,
+                        moe_stream_t stream) {
+  Dims D;
+  TRY(check_config(cfg, &D));
+  TRY(check_ptrs({x, topk_idx, gate, score, counts_raw, counts_kept, offsets, row_of, row_token, row_gate, x_perm,
+                  ws},
+                 "moe_dispatch"));
+  moe_workspace_layout L;
+  make_layout(D, &L);
+  return do_dispatch(D, L, x, topk_idx, gate, score, counts_raw, counts_kept, offsets, row_of, row_token, row_gate,
+                     x_perm, ws, (cudaStream_t)stream);
+}
+
+moe_status moe_expert_ffn(const moe_config *cfg, const void *x_perm, const int32_t *offsets, const void *w1,
+                          const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
+                          float *y_perm, void *ws, moe_stream_t stream) {
+  Dims D;
+  TRY(check_config(cfg, &D));
+  TRY(check_ptrs({x_perm, offsets, w1, b1, w2, b2, y_perm, ws}, "moe_expert_ffn"));
+  TRY(check_opt(row_gate, "moe_expert_ffn row_gate"));
+  TRY(check_opt(h, "moe_expert_ffn h"));
+  moe_workspace_layout L;
+  make_layout(D, &L);
+  if (!h) h = AT(ws, L.h, void *);
+  return do_ffn(D, L, x_perm, offsets, w1, b1, w2, b2, row_gate, h, y_perm, ws, (cudaStream_t)stream);
+}
+
+moe_status moe_combine(const moe_config *cfg, const float *y_perm, const int32_t *row_of, const float *gate,
+                       const void *x, void *y, void *ws, moe_stream_t stream) {
+  Dims D;
+  TRY(check_config(cfg, &D));
+  TRY(check_ptrs({y_perm, row_of, y, ws}, "moe_combine"));
+  if ((D.flags & MOE_FLAG_RENORM_SURVIVORS)) TRY(check_ptrs({gate}, "moe_combine gate (renormalise flag)"));
+  if ((D.flags & MOE_FLAG_IDENTITY_FALLBACK)) TRY(check_ptrs({x}, "moe_combine x (identity fallback flag)"));
+  moe_workspace_layout L;
+  make_layout(D, &L);
+  return do_combine(D, L, y_perm, row_of, gate, x, y, ws, (cudaStream_t)stream);
+}
+
+moe_status moe_forward(const moe_config *cfg, const void *x, const void *w_g, const float *router_bias,
+                       const void *w1, const void *b1, const void *w2, const void *b2, void *y, void *ws,
+                       moe_stream_t stream) {
+  Dims D;
+  TRY(check_config(cfg, &D));
+  TRY(check_ptrs({x, w_g, w1, b1, w2, b2, y, ws}, "moe_forward"));
+  TRY(check_opt(router_bias, "moe_forward router_bias"));
+  moe_workspace_layout L;
+  make_layout(D, &L);
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t *topk_idx = AT(ws, L.topk_idx, int32_t *);
+  float *gate = AT(ws, L.gate, float *);
+  float *score = AT(ws, L.score, float *);
+  int32_t *offsets = AT(ws, L.offsets, int32_t *);
+  int32_t *row_of = AT(ws, L.row_of, int32_t *);
+  float *row_gate = AT(ws, L.row_gate, float *);
+  void *x_perm = AT(ws, L.x_perm, void *);
+  float *y_perm = AT(ws, L.y_perm, float *);
+  TRY(do_route(D, L, x, w_g, router_bias, topk_idx, gate, score, ws, s));
+  TRY(do_dispatch(D, L, x, topk_idx, gate, score, AT(ws, L.counts_raw, int32_t *), AT(ws, L.counts_kept, int32_t *),
+                  offsets, row_of, AT(ws, L.row_token, int32_t *), row_gate, x_perm, ws, s));
+  TRY(do_ffn(D, L, x_perm, offsets, w1, b1, w2, b2, row_gate, AT(ws, L.h, void *), y_perm, ws, s));
+  TRY(do_combine(D, L, y_perm, row_of, gate, x, y, ws, s));
+  return MOE_OK;
+}
+
+}  // extern "C"

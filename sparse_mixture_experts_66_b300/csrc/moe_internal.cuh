@@ -1,0 +1,93 @@
+// Internal declarations shared by the kernels and the C-ABI layer.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// Every expert segment of the permuted buffers starts on a multiple of this
+// many rows, so that a 128-row GEMM tile never spans two experts.
+constexpr int kRowAlign = 128;
+
+// Kernel ids recorded next to a device error code in the status word.
+enum KernelId : int32_t {
+  kKRouter = 1,
+  kKCapSelect = 2,
+  kKCapAssign = 3,
+  kKPermute = 4,
+  kKGemmSimt = 5,
+  kKCombine = 6,
+  kKGemmTc = 7,
+  kKGemmTcDecode = 8,
+};
+
+struct Dims {
+  int64_t T, d, d_ff;
+  int32_t N, k;
+  int64_t C;      // capacity
+  int64_t R_max;  // row capacity of the permuted buffers
+  moe_dtype dt;
+  uint32_t flags;
+};
+
+// Record the first device-side error: status[0] = code, status[1] = kernel,
+// status[2] = detail. Later errors leave the first one in place.
+__device__ __forceinline__ void report_error(int32_t *status, int32_t code, int32_t kernel, int32_t detail) {
+  if (atomicCAS(status, 0, code) == 0) {
+    status[1] = kernel;
+    status[2] = detail;
+  }
+}
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// Exact GELU, u * Phi(u), with CUDA's erff.
+__device__ __forceinline__ float gelu_erf(float u) { return 0.5f * u * (1.0f + erff(u * 0.70710678118654752440f)); }
+
+// The expert whose segment holds row r: offsets is non-decreasing, N+1 long.
+__device__ __forceinline__ int segment_of(const int32_t *offsets, int N, int64_t r) {
+  int lo = 0, hi = N - 1;
+  while (lo < hi) {  // largest e with offsets[e] <= r
+    int mid = (lo + hi + 1) >> 1;
+    if (offsets[mid] <= r) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// ---- launchers (each returns the launch's cudaError_t) ----
+cudaError_t launch_router(const Dims &D, const void *x, const void *w_g, const float *router_bias,
+                          int32_t *topk_idx, float *gate, float *score, int32_t *status, cudaStream_t s);
+
+cudaError_t launch_capacity(const Dims &D, const int32_t *topk_idx, const float *gate, const float *score,
+                            int32_t *counts_raw, int32_t *counts_kept, int32_t *offsets, uint32_t *sel_thr,
+                            int32_t *sel_eq, int32_t *row_of, int32_t *row_token, float *row_gate,
+                            int32_t *status, cudaStream_t s);
+
+cudaError_t launch_permute(const Dims &D, const void *x, const int32_t *offsets, const int32_t *row_token,
+                           void *x_perm, int32_t *status, cudaStream_t s);
+
+cudaError_t launch_combine(const Dims &D, const float *y_perm, const int32_t *row_of, const float *gate,
+                           const void *x, void *y, int32_t *status, cudaStream_t s);
+
+// Grouped GEMM over expert segments with the two fused epilogues.
+//   epi 1: out[r, n] = GELU(A[r] . B[e, n] + bias[e, n])            (dtype)
+//   epi 2: out[r, n] = row_gate[r] * (A[r] . B[e, n] + bias[e, n])  (fp32)
+cudaError_t launch_ffn_simt(const Dims &D, int epi, const void *A, int64_t K, const void *B, const void *bias,
+                            int64_t N_out, const float *row_gate, const int32_t *offsets, void *out,
+                            int32_t *status, cudaStream_t s);
+
+// tcgen05 path (bf16). Returns cudaErrorNotSupported when the shape is not
+// handled, so the caller can report MOE_ERR_UNSUPPORTED.
+cudaError_t launch_ffn_tc(const Dims &D, const void *x_perm, const int32_t *offsets, const void *w1,
+                          const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
+                          float *y_perm, int32_t *status, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,116 @@
+"""The C-ABI library loads and exports every declared symbol; host-side logic (CPU only)."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import oracle as O
+from sparse_mixture_experts_66_b300 import moe
+from sparse_mixture_experts_66_b300.workload import WORKLOADS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = moe.load()
+    declared = header_functions()
+    assert len(declared) >= 12
+    for name in declared:
+        assert hasattr(lib, name), name
+    # the binding knows the same set, under the same names
+    assert sorted(moe.SIGNATURES) == declared
+    for name in declared:
+        assert callable(getattr(moe, name))
+
+
+def test_version():
+    assert "sm_103a" in moe.moe_version()
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_capacity_matches_oracle_formula(name):
+    w = WORKLOADS[name]
+    cfg = moe.config_of(w)
+    assert moe.moe_capacity(cfg) == O.load().capacity(w.T, w.N, w.k, w.capacity_factor)
+
+
+def test_capacity_edge_values():
+    for T, N, k, cf, C in [(5, 4, 2, 0.8, 2), (10, 3, 1, 1.0, 4), (7, 2, 2, 100.0, 7), (100, 8, 2, math.inf, 100),
+                           (100, 8, 2, 0.0, 100), (100, 8, 2, -1.0, 100), (1, 1, 1, 1.0, 1)]:
+        cfg = moe.make_config(T, 8, 8, N, k, cf)
+        assert moe.moe_capacity(cfg) == C
+
+
+def test_workspace_layout_is_aligned_and_sized():
+    for w in WORKLOADS.values():
+        cfg = moe.config_of(w)
+        L = moe.moe_get_workspace_layout(cfg)
+        S = min(w.T * w.k, w.N * L.capacity)
+        assert L.rows == (S + 127 * w.N) // 128 * 128
+        offs = [getattr(L, f) for f, _ in moe.MoeWorkspaceLayout._fields_[:15]]
+        assert all(o % 256 == 0 for o in offs)
+        assert offs == sorted(offs)
+        es = 2 if w.dtype == "bf16" else 4
+        assert L.total >= L.y_perm + L.rows * w.d * 4
+        assert L.h - L.x_perm >= L.rows * w.d * es
+        assert moe.moe_workspace_bytes(cfg) == L.total
+
+
+@pytest.mark.parametrize("field,value", [("T", 0), ("N", 0), ("N", 257), ("k", 0), ("k", 9), ("d", 12),
+                                         ("d_ff", 4), ("dtype", 7), ("flags", 8)])
+def test_invalid_config_rejected_on_host(field, value):
+    cfg = moe.make_config(64, 64, 64, 8, 2, 1.25)
+    setattr(cfg, field, value)
+    assert moe.moe_workspace_bytes(cfg) == 0
+    assert moe.moe_capacity(cfg) == -1
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_get_workspace_layout(cfg)
+    assert ei.value.status == moe.MOE_ERR_INVALID_ARG
+
+
+def test_k_larger_than_N_rejected():
+    cfg = moe.make_config(64, 64, 64, 2, 3, 1.25)
+    assert moe.moe_workspace_bytes(cfg) == 0
+
+
+def test_null_and_misaligned_pointers_rejected_before_any_launch():
+    lib = moe.load()
+    cfg = moe.make_config(64, 64, 64, 8, 2, 1.25)
+    P = ctypes.c_void_p
+    st = lib.moe_route(ctypes.byref(cfg), None, None, None, None, None, None, None, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    assert b"NULL" in lib.moe_last_error()
+    # misaligned (never dereferenced: rejected on the host)
+    bad = P(0x1003)
+    st = lib.moe_forward(ctypes.byref(cfg), bad, bad, None, bad, bad, bad, bad, bad, bad, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    assert b"aligned" in lib.moe_last_error()
+    st = lib.moe_combine(ctypes.byref(cfg), None, None, None, None, None, None, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+
+
+def test_flag_variants_need_their_inputs():
+    lib = moe.load()
+    cfg = moe.make_config(64, 64, 64, 8, 2, 1.25, flags=moe.MOE_FLAG_RENORM_SURVIVORS)
+    p = ctypes.c_void_p(0x1000)
+    st = lib.moe_combine(ctypes.byref(cfg), p, p, None, None, p, p, None)
+    assert st == moe.MOE_ERR_INVALID_ARG and b"gate" in lib.moe_last_error()
+    cfg.flags = moe.MOE_FLAG_IDENTITY_FALLBACK
+    st = lib.moe_combine(ctypes.byref(cfg), p, p, None, None, p, p, None)
+    assert st == moe.MOE_ERR_INVALID_ARG and b"x" in lib.moe_last_error()
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    cfg = moe.make_config(8, 8, 8, 2, 1, 1.0, dtype=torch.float32)
+    x = torch.zeros(8, 8)
+    with pytest.raises(ValueError, match="CUDA"):
+        moe.moe_forward(cfg, x, x, None, x, x, x, x, x, x, stream=None)

@@ -1,0 +1,50 @@
+"""Host-side logic of bench.py (CPU only): the replica aggregation over ranks
+with gloo at world size 2, and the reference arm's JSON line."""
+import json
+import os
+import subprocess
+import sys
+
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    sys.path.insert(0, ROOT)
+    import bench
+
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    seconds = [0.010, 0.025][rank]
+    value, slowest = bench.aggregate_throughput(1000.0, seconds, world, torch.device("cpu"))
+    out[rank] = (value, slowest)
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_replica_throughput_takes_the_slowest_rank():
+    port = 29500 + os.getpid() % 1000
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_rank_main, args=(2, port, out), nprocs=2, join=True)
+        res = dict(out)
+    for r in (0, 1):
+        value, slowest = res[r]
+        assert abs(slowest - 0.025) < 1e-12
+        assert abs(value - 2000.0 / 0.025) < 1e-6
+
+
+def test_reference_arm_prints_one_json_line():
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2", "--warmup", "1",
+           "--workload", "f32_T256_d64_N4_k1_dff256_cf1.25", "--ref-budget", "3"]
+    p = subprocess.run(cmd, capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [l for l in p.stdout.strip().splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "tokens/s"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0

@@ -1,0 +1,206 @@
+"""CUDA path against the CPU oracle, through the C ABI (needs a B300)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from sparse_mixture_experts_66_b300 import moe
+from sparse_mixture_experts_66_b300.workload import (DECODE, HEADLINE, PREFILL, SKEWED, SMALL_FP32, WORKLOADS,
+                                                     as_f32_numpy, custom, draw)
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.fail("no CUDA device: the GPU tests need a B300")
+    moe.load()
+    yield
+    torch.cuda.synchronize()
+
+
+# ---------------------------------------------------------------------------
+# Stage-isolated checks
+# ---------------------------------------------------------------------------
+STAGE_CASES = [
+    custom(1000, 256, 1408, 8, 2, 1.25, seed=1),
+    custom(777, 512, 384, 6, 2, 1.0, router_bias="zipf", seed=2),
+    custom(300, 128, 64, 64, 2, 1.0, router_bias="zipf", seed=3),
+    custom(256, 64, 256, 4, 1, 1.25, dtype="f32", seed=0),
+    custom(512, 64, 64, 256, 8, 1.0, seed=4),
+]
+
+
+@pytest.mark.parametrize("w", STAGE_CASES, ids=lambda w: w.name)
+def test_capacity_stage_is_bit_exact_on_gpu_routing(w):
+    """The oracle's capacity step, run on the GPU's own picks and fp32 scores,
+    must reproduce the GPU's counts, slots and drops exactly."""
+    inp = draw(w)
+    g = parity.run_gpu(w, inp)
+    cr, ck, slot = O.load().capacity_assign(g["topk_idx"], g["score"].astype(np.float64), w.N,
+                                            O.load().capacity(w.T, w.N, w.k, w.capacity_factor))
+    assert np.array_equal(cr, g["counts_raw"])
+    assert np.array_equal(ck, g["counts_kept"])
+    assert np.array_equal(slot, parity.gpu_slots(g))
+    parity.check_layout(g, w.k)
+
+
+@pytest.mark.parametrize("w", STAGE_CASES[:3], ids=lambda w: w.name)
+def test_permute_is_an_exact_gather(w):
+    inp = draw(w)
+    g = parity.run_gpu(w, inp)
+    xp = g["_ws"].views()["x_perm"].cpu()
+    rows = int(g["offsets"][-1])
+    rt = torch.from_numpy(g["row_token"][:rows]).long()
+    x = inp["x"]
+    used = rt >= 0
+    assert torch.equal(xp[:rows][used], x[rt[used]])
+    assert torch.all(xp[:rows][~used] == 0)
+
+
+@pytest.mark.parametrize("w", STAGE_CASES[:3], ids=lambda w: w.name)
+def test_combine_is_the_fixed_order_fp32_sum(w):
+    """y[t] = sum over kept picks in pick order of y_perm rows, in fp32, then
+    rounded once to the storage dtype: reproduced bit for bit."""
+    inp = draw(w)
+    g = parity.run_gpu(w, inp)
+    yp = g["_ws"].views()["y_perm"].cpu().numpy()
+    acc = np.zeros((w.T, w.d), dtype=np.float32)
+    for j in range(w.k):
+        r = g["row_of"][:, j]
+        m = r >= 0
+        acc[m] = acc[m] + yp[r[m]]
+    ref = torch.from_numpy(acc).to(g["_y"].dtype)
+    assert torch.equal(g["_y"].cpu(), ref)
+
+
+@pytest.mark.parametrize("w", STAGE_CASES[:3], ids=lambda w: w.name)
+def test_expert_ffn_rows_against_oracle(w):
+    """Each permuted row's y_perm equals row_gate * E_e(x_perm row) (oracle, fp64)."""
+    inp = draw(w)
+    g = parity.run_gpu(w, inp)
+    v = g["_ws"].views()
+    xp = v["x_perm"].float().cpu().numpy()
+    yp = v["y_perm"].cpu().numpy()
+    off = g["offsets"]
+    w1, b1, w2, b2 = (as_f32_numpy(inp[n]) for n in ("w1", "b1", "w2", "b2"))
+    rng = np.random.default_rng(0)
+    orc = O.load()
+    rows = int(off[-1])
+    check = rng.choice(rows, size=min(rows, 96), replace=False)
+    errs, scale = [], []
+    for r in check:
+        e = int(np.searchsorted(off, r, side="right") - 1)
+        if g["row_token"][r] < 0:
+            continue
+        ref = g["row_gate"][r] * orc.expert_ffn(xp[r], w1[e], b1[e], w2[e], b2[e])
+        errs.append(np.max(np.abs(yp[r] - ref)))
+        scale.append(np.max(np.abs(ref)))
+    assert max(errs) <= parity.TOL[w.dtype] * max(scale)
+
+
+def test_router_against_oracle():
+    w = custom(2048, 1024, 64, 8, 2, math.inf, seed=5)
+    inp = draw(w)
+    g = parity.run_gpu(w, inp)
+    ref = parity.oracle_ref(w, inp, sel=np.array([0]))
+    mg = parity.margins(ref["logits"], w.k)
+    hi = mg > parity.MARGIN
+    assert np.array_equal(g["topk_idx"][hi], ref["idx"][hi])
+    assert np.allclose(g["gate"], ref["gate"], rtol=2e-5, atol=1e-6)
+    assert np.allclose(g["gate"].sum(axis=1), 1.0, atol=1e-6)
+
+
+# ---------------------------------------------------------------------------
+# End to end, every output element, small sizes spanning several tiles
+# ---------------------------------------------------------------------------
+E2E_CASES = [
+    WORKLOADS[SMALL_FP32],
+    custom(1000, 256, 1408, 8, 2, 1.25, seed=1),  # ragged d_ff tile, segments not multiples of 128
+    custom(777, 512, 384, 6, 2, 1.0, router_bias="zipf", seed=2),  # skewed: drops
+    custom(300, 128, 64, 64, 2, 1.0, router_bias="zipf", seed=3),  # d_ff below one tile, many experts
+    custom(1, 256, 512, 8, 2, 1.25, seed=6),  # a single token
+    custom(200, 128, 256, 1, 1, 1.0, seed=7),  # N = 1, k = 1: a dense FFN
+    custom(200, 64, 64, 1, 1, 1.0, dtype="f32", seed=7),
+    custom(130, 128, 256, 4, 4, math.inf, seed=8),  # k = N: the full soft mixture
+    custom(512, 64, 64, 256, 8, 1.0, seed=4),  # the largest N and k
+    custom(400, 128, 256, 8, 2, 1.0, router_bias="const:0:30", seed=9),  # every token wants expert 0
+    custom(640, 128, 128, 8, 2, 0.01, seed=10),  # tiny capacity: nearly everything dropped
+    custom(333, 64, 128, 8, 2, 1.25, router_bias="const:3:-60", seed=11),  # an expert nobody picks
+    custom(256, 64, 256, 4, 1, 1.25, dtype="f32", router_bias="zipf", seed=12),  # fp32 with drops
+]
+
+
+@pytest.mark.parametrize("w", E2E_CASES, ids=lambda w: w.name)
+def test_end_to_end(w):
+    rep, g, ref, _ = parity.full_check(w)
+    print(w.name, rep)
+
+
+@pytest.mark.parametrize("flags", [moe.MOE_FLAG_RENORM_SURVIVORS, moe.MOE_FLAG_IDENTITY_FALLBACK, 3])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_flag_variants(flags, dtype):
+    w = custom(500, 128, 256, 8, 2, 0.5, dtype=dtype, router_bias="zipf", seed=13)
+    rep, g, ref, _ = parity.full_check(w, flags=flags)
+    assert rep["dropped"] > 0
+    print(w.name, flags, rep)
+
+
+def test_deterministic_across_runs():
+    w = custom(1500, 256, 512, 8, 2, 1.0, router_bias="zipf", seed=14)
+    inp = draw(w)
+    a = parity.run_gpu(w, inp)
+    b = parity.run_gpu(w, inp, dev=a["_dev"], reps=3)
+    assert torch.equal(a["_y"], b["_y"])
+    assert np.array_equal(a["row_of"], b["row_of"])
+
+
+def test_stage_calls_compose_to_forward():
+    """moe_route + moe_dispatch + moe_expert_ffn + moe_combine on caller
+    buffers give the same bits as moe_forward."""
+    w = custom(700, 256, 512, 8, 2, 1.0, router_bias="zipf", seed=15)
+    inp = draw(w)
+    g = parity.run_gpu(w, inp)
+    dev, cfg = g["_dev"], g["_cfg"]
+    L = moe.moe_get_workspace_layout(cfg)
+    ws = moe.Workspace(cfg)
+    T, k, N, R = w.T, w.k, w.N, L.rows
+    i32 = dict(dtype=torch.int32, device="cuda")
+    f32 = dict(dtype=torch.float32, device="cuda")
+    topk_idx, gate, score = torch.empty(T, k, **i32), torch.empty(T, k, **f32), torch.empty(T, k, **f32)
+    moe.moe_route(cfg, dev["x"], dev["w_g"], dev["router_bias"], topk_idx, gate, score, ws.buf)
+    counts_raw, counts_kept, offsets = torch.empty(N, **i32), torch.empty(N, **i32), torch.empty(N + 1, **i32)
+    row_of, row_token, row_gate = torch.empty(T, k, **i32), torch.empty(R, **i32), torch.empty(R, **f32)
+    x_perm = torch.empty(R, w.d, dtype=dev["x"].dtype, device="cuda")
+    moe.moe_dispatch(cfg, dev["x"], topk_idx, gate, score, counts_raw, counts_kept, offsets, row_of, row_token,
+                     row_gate, x_perm, ws.buf)
+    h = torch.empty(R, w.d_ff, dtype=dev["x"].dtype, device="cuda")
+    y_perm = torch.empty(R, w.d, **f32)
+    moe.moe_expert_ffn(cfg, x_perm, offsets, dev["w1"], dev["b1"], dev["w2"], dev["b2"], row_gate, h, y_perm, ws.buf)
+    y = torch.empty_like(dev["x"])
+    moe.moe_combine(cfg, y_perm, row_of, gate, dev["x"], y, ws.buf)
+    ws.status()
+    assert torch.equal(y, g["_y"])
+    assert np.array_equal(row_of.cpu().numpy(), g["row_of"])
+
+
+def test_device_status_is_clean_after_runs():
+    w = custom(64, 64, 64, 4, 2, 1.0, seed=16)
+    g = parity.run_gpu(w, draw(w))
+    g["_ws"].status()
+
+
+# ---------------------------------------------------------------------------
+# The published workloads at full size: routing and capacity on every token,
+# outputs on a sample of tokens (cutoff tokens, dropped tokens, random tokens)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("name", [HEADLINE, SKEWED, DECODE, PREFILL])
+def test_full_size_workloads(name):
+    w = WORKLOADS[name]
+    rep, g, ref, _ = parity.full_check(w, sample=48)
+    print(name, rep)
+    torch.cuda.empty_cache()
