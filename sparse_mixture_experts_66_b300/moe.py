@@ -74,7 +74,7 @@ SIGNATURES = {
     "moe_get_device_status": (["P", "S"], ctypes.c_int),
     "moe_route": (["C"] + ["P"] * 7 + ["S"], ctypes.c_int),
     "moe_dispatch": (["C"] + ["P"] * 12 + ["S"], ctypes.c_int),
-    "moe_expert_ffn": (["C"] + ["P"] * 11 + ["S"], ctypes.c_int),
+    "moe_expert_ffn": (["C"] + ["P"] * 10 + ["S"], ctypes.c_int),
     "moe_combine": (["C"] + ["P"] * 6 + ["S"], ctypes.c_int),
     "moe_forward": (["C"] + ["P"] * 9 + ["S"], ctypes.c_int),
 }

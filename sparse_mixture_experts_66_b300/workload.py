@@ -67,8 +67,9 @@ SKEWED = "bf16_T8192_d2048_N64_k2_dff1408_cf1.0_zipf"
 DECODE = "bf16_T64_d4096_N8_k2_dff14336_nocap"
 
 
-def custom(T, d, N, k, d_ff, capacity_factor, dtype="bf16", router_bias="none", seed=0) -> Workload:
-    """A workload of any shape with the same input law (used by parity tests)."""
+def custom(T, d, d_ff, N, k, capacity_factor, dtype="bf16", router_bias="none", seed=0) -> Workload:
+    """A workload of any shape with the same input law (used by parity tests).
+    Argument order follows the C config: T, d, d_ff, N, k."""
     name = f"{dtype}_T{T}_d{d}_N{N}_k{k}_dff{d_ff}_cf{capacity_factor}_{router_bias}_s{seed}"
     return Workload(name, dtype, T, d, N, k, d_ff, capacity_factor, router_bias, seed)
 

@@ -31,6 +31,23 @@ def test_library_exports_every_declared_symbol():
         assert callable(getattr(moe, name))
 
 
+def header_prototypes():
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(moe_[a-z_]+)\s*\(([^)]*)\)\s*;", text):
+        args = m.group(2).strip()
+        out[m.group(1)] = 0 if args in ("", "void") else args.count(",") + 1
+    return out
+
+
+def test_binding_argument_counts_match_the_header():
+    protos = header_prototypes()
+    assert sorted(protos) == header_functions()
+    for name, n in protos.items():
+        assert len(moe.SIGNATURES[name][0]) == n, name
+
+
 def test_version():
     assert "sm_103a" in moe.moe_version()
 

@@ -32,6 +32,8 @@ STAGE_CASES = [
     custom(300, 128, 64, 64, 2, 1.0, router_bias="zipf", seed=3),
     custom(256, 64, 256, 4, 1, 1.25, dtype="f32", seed=0),
     custom(512, 64, 64, 256, 8, 1.0, seed=4),
+    # every fp32 score of expert 0 rounds to 1.0: a full tie, resolved by token order
+    custom(400, 128, 256, 8, 2, 1.0, router_bias="const:0:30", seed=9),
 ]
 
 
@@ -128,7 +130,7 @@ E2E_CASES = [
     custom(200, 64, 64, 1, 1, 1.0, dtype="f32", seed=7),
     custom(130, 128, 256, 4, 4, math.inf, seed=8),  # k = N: the full soft mixture
     custom(512, 64, 64, 256, 8, 1.0, seed=4),  # the largest N and k
-    custom(400, 128, 256, 8, 2, 1.0, router_bias="const:0:30", seed=9),  # every token wants expert 0
+    custom(400, 128, 256, 8, 2, 1.0, router_bias="const:0:3", seed=9),  # most tokens want expert 0
     custom(640, 128, 128, 8, 2, 0.01, seed=10),  # tiny capacity: nearly everything dropped
     custom(333, 64, 128, 8, 2, 1.25, router_bias="const:3:-60", seed=11),  # an expert nobody picks
     custom(256, 64, 256, 4, 1, 1.25, dtype="f32", router_bias="zipf", seed=12),  # fp32 with drops
