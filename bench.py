@@ -85,7 +85,8 @@ def max_over_ranks(value: float, world: int, device) -> float:
 
 
 def aggregate_throughput(units_per_rank: float, seconds_per_rank: float, world: int, device) -> tuple:
-    """Whole-job throughput of replicas: all ranks' units over the slowest rank's time."""
+    """Whole-job throughput of replicas: the units every rank processed in one
+    step (tokens), summed over ranks, over the slowest rank's step time."""
     slowest = max_over_ranks(seconds_per_rank, world, device)
     return units_per_rank * world / slowest, slowest
 
@@ -245,7 +246,7 @@ def run_ours(args, world, rank, local):
     stage_ms = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev)
                 for j, n in enumerate(["route", "dispatch", "expert_ffn", "combine"])}
     ms = statistics.mean(step_ms)
-    value, slowest_s = aggregate_throughput(w.T / (ms * 1e-3), ms * 1e-3, world, device)
+    value, slowest_s = aggregate_throughput(w.T, ms * 1e-3, world, device)
     ms_max = slowest_s * 1e3
 
     # end to end through moe_forward with host buffers
@@ -273,7 +274,7 @@ def run_ours(args, world, rank, local):
     barrier(world)
     ws.status(stream)
     e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)
-    e2e_value, _ = aggregate_throughput(w.T / (e2e_ms * 1e-3), e2e_ms * 1e-3, world, device)
+    e2e_value, _ = aggregate_throughput(w.T, e2e_ms * 1e-3, world, device)
     es = 2 if w.dtype == "bf16" else 4
 
     peaks, peak_src = load_peaks()

@@ -144,6 +144,13 @@ moe_status do_ffn(const Dims &D, const moe_workspace_layout &L, const void *x_pe
                   const void *w1, const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
                   float *y_perm, void *ws, cudaStream_t s) {
   int32_t *status = AT(ws, L.status, int32_t *);
+  if (D.dt == MOE_DT_BF16) {
+    cudaError_t e = launch_ffn_tc(D, x_perm, offsets, w1, b1, w2, b2, row_gate, h, y_perm, status, s);
+    if (e == cudaErrorNotSupported)
+      return fail(MOE_ERR_UNSUPPORTED, "expert FFN: shape not supported by the tensor-core kernels");
+    if (e != cudaSuccess) return cuda_fail(e, "expert FFN (tensor cores)");
+    return MOE_OK;
+  }
   cudaError_t e = launch_ffn_simt(D, 1, x_perm, D.d, w1, b1, D.d_ff, nullptr, offsets, h, status, s);
   if (e != cudaSuccess) return cuda_fail(e, "expert GEMM1 launch");
   e = launch_ffn_simt(D, 2, h, D.d_ff, w2, b2, D.d, row_gate, offsets, y_perm, status, s);
