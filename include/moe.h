@@ -192,6 +192,25 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const void *w_g, co
                        const void *w1, const void *b1, const void *w2, const void *b2, void *y, void *ws,
                        moe_stream_t stream);
 
+/* The layer forward for callers that cannot allocate device memory (plugin
+ * or custom-op hosts that provide inputs and outputs but no workspace, code
+ * whose memory belongs to an allocator that forbids direct cudaMalloc, or
+ * paths that must avoid cudaMalloc's device synchronisation). The pages have
+ * no counterpart: this is a property of the library, not of the method.
+ * Same arguments and result as moe_forward, minus the workspace: the scratch
+ * is a file-scope device array of 32 MiB that every GPU loading the library
+ * keeps until the process exits. Configs whose moe_workspace_bytes exceeds
+ * 32 MiB return MOE_ERR_WORKSPACE before anything is enqueued. The first call
+ * on a device looks up the array's address (once per device): make it before
+ * any stream capture. All calls share the array and it keeps the last call's
+ * contents; each call clears its status word first. Calls whose GPU work
+ * overlaps race. Device-side errors are not readable afterwards (the status
+ * word is not the caller's): only host-side errors are returned. Never
+ * allocates. */
+moe_status moe_forward_noalloc(const moe_config *cfg, const void *x, const void *w_g, const float *router_bias,
+                               const void *w1, const void *b1, const void *w2, const void *b2, void *y,
+                               moe_stream_t stream);
+
 #if defined(__GNUC__)
 #pragma GCC visibility pop
 #endif

@@ -167,6 +167,8 @@ moe_status do_combine(const Dims &D, const moe_workspace_layout &L, const float 
 
 }  // namespace
 
+void moe::set_last_error(const char *text) { snprintf(g_err, sizeof(g_err), "%s", text); }
+
 extern "C" {
 
 const char *moe_version(void) { return "sparse-moe-b300 0.1 (sm_103a)"; }

@@ -62,6 +62,9 @@ __device__ __forceinline__ int segment_of(const int32_t *offsets, int N, int64_t
   return lo;
 }
 
+// Replace the calling thread's moe_last_error() text.
+void set_last_error(const char *text);
+
 // ---- launchers (each returns the launch's cudaError_t) ----
 cudaError_t launch_router(const Dims &D, const void *x, const void *w_g, const float *router_bias,
                           int32_t *topk_idx, float *gate, float *score, int32_t *status, cudaStream_t s);

@@ -77,6 +77,7 @@ SIGNATURES = {
     "moe_expert_ffn": (["C"] + ["P"] * 10 + ["S"], ctypes.c_int),
     "moe_combine": (["C"] + ["P"] * 6 + ["S"], ctypes.c_int),
     "moe_forward": (["C"] + ["P"] * 9 + ["S"], ctypes.c_int),
+    "moe_forward_noalloc": (["C"] + ["P"] * 8 + ["S"], ctypes.c_int),
 }
 _KIND = {"C": ctypes.POINTER(MoeConfig), "P": ctypes.c_void_p, "S": ctypes.c_void_p,
          "L": ctypes.POINTER(MoeWorkspaceLayout)}
@@ -194,6 +195,15 @@ def moe_combine(cfg, y_perm, row_of, gate, x, y, ws, stream=None):
 def moe_forward(cfg, x, w_g, router_bias, w1, b1, w2, b2, y, ws, stream=None):
     _check(load().moe_forward(ctypes.byref(cfg), _ptr(x), _ptr(w_g), _ptr(router_bias), _ptr(w1), _ptr(b1),
                               _ptr(w2), _ptr(b2), _ptr(y), _ptr(ws), _stream(stream)))
+
+
+def moe_forward_noalloc(cfg, x, w_g, router_bias, w1, b1, w2, b2, y, stream=None):
+    """moe_forward without a workspace, for callers that cannot allocate device
+    memory: the library's fixed 32 MiB device scratch array is used instead.
+    Larger configs raise MOE_ERR_WORKSPACE; calls that overlap on the GPU race
+    on the shared array."""
+    _check(load().moe_forward_noalloc(ctypes.byref(cfg), _ptr(x), _ptr(w_g), _ptr(router_bias), _ptr(w1), _ptr(b1),
+                                      _ptr(w2), _ptr(b2), _ptr(y), _stream(stream)))
 
 
 # ---- workspace helper -------------------------------------------------------
