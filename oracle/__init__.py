@@ -127,6 +127,16 @@ class Oracle:
                                             self._ptr(ck), self._ptr(slot))
         return cr, ck, slot
 
+    def expert_ffn_hidden(self, xrow, w1e, b1e, w2e, b2e):
+        """(h, out) of one expert on one row: h = GELU(W1 x + b1) (exact erf), out = W2 h + b2."""
+        xrow, w1e, b1e, w2e, b2e = (self._f32(a) for a in (xrow, w1e, b1e, w2e, b2e))
+        d_ff, d = w1e.shape
+        h = np.empty(d_ff, dtype=np.float64)
+        out = np.empty(d, dtype=np.float64)
+        self.lib.moe_oracle_expert_ffn(d, d_ff, self._ptr(xrow), self._ptr(w1e), self._ptr(b1e), self._ptr(w2e),
+                                       self._ptr(b2e), self._ptr(h), self._ptr(out))
+        return h, out
+
     def expert_ffn(self, xrow, w1e, b1e, w2e, b2e):
         xrow, w1e, b1e, w2e, b2e = (self._f32(a) for a in (xrow, w1e, b1e, w2e, b2e))
         d_ff, d = w1e.shape

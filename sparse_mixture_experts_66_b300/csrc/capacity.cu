@@ -7,15 +7,17 @@
 // requests fill the expert's buffer in token order (the pseudocode's
 // expert_buffer), which fixes each request's slot.
 //
-// Two launches, one CTA per expert each, no atomics on any output:
-//   select: count the expert's requests; if the count exceeds C, radix-select
-//           (4 passes of 8 bits over the fp32 score's bit pattern, which orders
-//           non-negative floats) the C-th largest score and how many requests
-//           equal to it must still be kept;
-//   assign: the segment of expert e starts at the sum of the earlier experts'
-//           kept counts, each rounded up to 128 rows; a block-wide scan in token
-//           order over "kept" flags numbers the kept rows; ties at the
-//           threshold are kept in token order until the quota is used.
+// One launch, one CTA per expert, no atomics deciding any output:
+//   1. every CTA counts the requests of all N experts (warp-aggregated with
+//      match_any into per-warp rows of a shared histogram), so each CTA can
+//      compute every segment offset itself: offset[e] = sum over e' < e of
+//      roundup(min(count[e'], C), 128). No CTA waits for another;
+//   2. if its expert overflows, the CTA radix-selects (4 passes of 8 bits over
+//      the fp32 score's bit pattern, which orders non-negative floats) the C-th
+//      largest score and how many requests equal to it are still kept;
+//   3. a block-wide scan in token order over "kept" flags numbers the kept
+//      rows; ties at the threshold are kept in token order until the quota is
+//      used. Padding rows of the segment get token -1 and gate 0.
 #include <limits.h>
 
 #include "moe_internal.cuh"
@@ -24,22 +26,10 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 1024;
-constexpr int kItems = 8;  // consecutive requests per thread in the assign pass
+constexpr int kWarps = kThreads / 32;
+constexpr int kItems = 8;  // consecutive requests per thread
 
 __device__ __forceinline__ int64_t round_up_rows(int64_t v) { return (v + kRowAlign - 1) / kRowAlign * kRowAlign; }
-
-__device__ __forceinline__ int block_sum(int v, int *s_red) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  if (lane == 0) s_red[w] = v;
-  __syncthreads();
-  int t = lane < (int)(blockDim.x >> 5) ? s_red[lane] : 0;
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
-  __syncthreads();
-  return t;
-}
 
 // Exclusive scan over the block in thread order; *total gets the block sum.
 __device__ __forceinline__ int block_exclusive_scan(int v, int *s_warp, int *total) {
@@ -68,110 +58,176 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *s_warp, int *tot
   return before + incl - v;
 }
 
-__global__ void __launch_bounds__(kThreads) cap_select_kernel(const int32_t *__restrict__ idx,
-                                                              const float *__restrict__ score, int64_t n, int64_t C,
-                                                              int32_t *counts_raw, int32_t *counts_kept,
-                                                              uint32_t *sel_thr, int32_t *sel_eq) {
-  __shared__ int s_hist[256];
-  __shared__ int s_red[32];
-  __shared__ uint32_t s_prefix;
-  __shared__ int s_need;
-  const int e = blockIdx.x;
-  int cnt = 0;
-  for (int64_t i = threadIdx.x; i < n; i += kThreads) cnt += (idx[i] == e);
-  const int count = block_sum(cnt, s_red);
-  if ((int64_t)count <= C) {
-    if (threadIdx.x == 0) {
-      counts_raw[e] = count;
-      counts_kept[e] = count;
-      sel_thr[e] = 0u;
-      sel_eq[e] = INT_MAX;
-    }
-    return;
-  }
-  uint32_t prefix = 0u, mask = 0u;
-  int need = (int)C;  // rank (from the top) of the wanted score among those matching prefix
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += kThreads) s_hist[i] = 0;
-    __syncthreads();
-    for (int64_t i = threadIdx.x; i < n; i += kThreads) {
-      if (idx[i] != e) continue;
-      const uint32_t b = __float_as_uint(score[i]);
-      if ((b & mask) == prefix) atomicAdd(&s_hist[(b >> shift) & 255u], 1);
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      int above = 0, D = 255;
-      for (; D > 0; --D) {
-        if (above + s_hist[D] >= need) break;
-        above += s_hist[D];
-      }
-      s_prefix = prefix | ((uint32_t)D << shift);
-      s_need = need - above;
-    }
-    __syncthreads();
-    prefix = s_prefix;
-    need = s_need;
-    mask |= 255u << shift;
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) {
-    counts_raw[e] = count;
-    counts_kept[e] = (int)C;
-    sel_thr[e] = prefix;  // bit pattern of the C-th largest score
-    sel_eq[e] = need;     // requests with exactly that score still kept, in token order
-  }
-}
+// The requests [i0, i0 + kItems) of one thread: expert, score bits, gate.
+struct Items {
+  int32_t ie[kItems];
+  uint32_t b[kItems];
+  float g[kItems];
+};
 
-__global__ void __launch_bounds__(kThreads) cap_assign_kernel(
-    const int32_t *__restrict__ idx, const float *__restrict__ gate, const float *__restrict__ score, int64_t n,
-    int k, int N, int64_t C, const int32_t *__restrict__ counts_raw, const int32_t *__restrict__ counts_kept,
-    const uint32_t *__restrict__ sel_thr, const int32_t *__restrict__ sel_eq, int32_t *offsets, int32_t *row_of,
-    int32_t *row_token, float *row_gate, int64_t R_max, int32_t *status) {
-  __shared__ int s_warp[32];
-  __shared__ int64_t s_off;
-  const int e = blockIdx.x;
-  if (threadIdx.x == 0) {
-    int64_t off = 0;
-    for (int j = 0; j < e; ++j) off += round_up_rows(counts_kept[j]);
-    s_off = off;
-    offsets[e] = (int32_t)off;
-    if (e == N - 1) offsets[N] = (int32_t)(off + round_up_rows(counts_kept[e]));
-  }
-  __syncthreads();
-  const int64_t off = s_off;
-  const int kept_e = counts_kept[e];
-  if (off + round_up_rows(kept_e) > R_max) {  // cannot happen for consistent inputs
-    if (threadIdx.x == 0) report_error(status, MOE_ERR_BOUNDS, kKCapAssign, e);
-    return;
-  }
-  const bool overflow = (int64_t)counts_raw[e] > C;
-  const uint32_t thr = sel_thr[e];
-  const int eq_keep = sel_eq[e];
-  int run_eq = 0, run_kept = 0;
-  for (int64_t base = 0; base < n; base += (int64_t)kThreads * kItems) {
-    const int64_t i0 = base + (int64_t)threadIdx.x * kItems;
-    int32_t ie[kItems];
-    uint32_t b[kItems];
-    int my_eq = 0;
+__device__ __forceinline__ void load_items(const int32_t *__restrict__ idx, const float *__restrict__ score,
+                                           const float *__restrict__ gate, int64_t n, int64_t i0, Items &it) {
+  if (i0 + kItems <= n) {  // i0 is a multiple of 8: 32-byte aligned vectors, all issued together
+    const int4 a0 = __ldg(reinterpret_cast<const int4 *>(idx + i0));
+    const int4 a1 = __ldg(reinterpret_cast<const int4 *>(idx + i0 + 4));
+    const uint4 s0 = __ldg(reinterpret_cast<const uint4 *>(score + i0));
+    const uint4 s1 = __ldg(reinterpret_cast<const uint4 *>(score + i0 + 4));
+    const float4 g0 = __ldg(reinterpret_cast<const float4 *>(gate + i0));
+    const float4 g1 = __ldg(reinterpret_cast<const float4 *>(gate + i0 + 4));
+    it.ie[0] = a0.x; it.ie[1] = a0.y; it.ie[2] = a0.z; it.ie[3] = a0.w;
+    it.ie[4] = a1.x; it.ie[5] = a1.y; it.ie[6] = a1.z; it.ie[7] = a1.w;
+    it.b[0] = s0.x; it.b[1] = s0.y; it.b[2] = s0.z; it.b[3] = s0.w;
+    it.b[4] = s1.x; it.b[5] = s1.y; it.b[6] = s1.z; it.b[7] = s1.w;
+    it.g[0] = g0.x; it.g[1] = g0.y; it.g[2] = g0.z; it.g[3] = g0.w;
+    it.g[4] = g1.x; it.g[5] = g1.y; it.g[6] = g1.z; it.g[7] = g1.w;
+  } else {
 #pragma unroll
     for (int q = 0; q < kItems; ++q) {
       const int64_t i = i0 + q;
-      ie[q] = i < n ? idx[i] : -1;
-      b[q] = (ie[q] == e) ? __float_as_uint(score[i]) : 0u;
-      my_eq += (ie[q] == e && overflow && b[q] == thr);
+      it.ie[q] = i < n ? idx[i] : -1;
+      it.b[q] = i < n ? __float_as_uint(score[i]) : 0u;
+      it.g[q] = i < n ? gate[i] : 0.f;
     }
-    int tot_eq;
-    int eq_rank = block_exclusive_scan(my_eq, s_warp, &tot_eq) + run_eq;
+  }
+}
+
+// kResident: all T*k requests fit one pass of kThreads * kItems, so they are
+// loaded once and every phase works from registers.
+template <bool kResident>
+__global__ void __launch_bounds__(kThreads) capacity_kernel(
+    const int32_t *__restrict__ idx, const float *__restrict__ gate, const float *__restrict__ score, int64_t n,
+    int k, int N, int64_t C, int32_t *counts_raw, int32_t *counts_kept, int32_t *offsets, int32_t *row_of,
+    int32_t *row_token, float *row_gate, int64_t R_max, int32_t *status) {
+  extern __shared__ int s_hist[];  // [kWarps][N]
+  __shared__ int s_warp[32];
+  __shared__ int s_sel[256];
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_need;
+  __shared__ int64_t s_off, s_end;
+  __shared__ int s_count;
+  const int e = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int64_t kChunk = (int64_t)kThreads * kItems;
+  const int64_t my0 = (int64_t)threadIdx.x * kItems;
+
+  Items it;
+  if (kResident) load_items(idx, score, gate, n, my0, it);
+
+  // 1. histogram of every expert's requests
+  for (int i = threadIdx.x; i < kWarps * N; i += kThreads) s_hist[i] = 0;
+  __syncthreads();
+  for (int64_t base = 0; base < n; base += kChunk) {
+    if (!kResident) load_items(idx, score, gate, n, base + my0, it);
+#pragma unroll
+    for (int q = 0; q < kItems; ++q) {
+      const int ex = it.ie[q];
+      const unsigned peers = __match_any_sync(0xffffffffu, ex);
+      if (ex >= 0 && ex < N && lane == __ffs(peers) - 1) s_hist[warp * N + ex] += __popc(peers);
+    }
+  }
+  __syncthreads();
+  int padded = 0, cnt = 0;
+  if (threadIdx.x < N) {
+    for (int w = 0; w < kWarps; ++w) cnt += s_hist[w * N + threadIdx.x];
+    padded = (int)round_up_rows(cnt < C ? cnt : C);
+  }
+  int total_rows;
+  const int excl = block_exclusive_scan(padded, s_warp, &total_rows);
+  if (threadIdx.x == e) {
+    s_off = excl;
+    s_end = (int64_t)excl + padded;
+    s_count = cnt;
+  }
+  __syncthreads();
+  const int64_t off = s_off;
+  const int count = s_count;
+  const int kept_e = (int64_t)count < C ? count : (int)C;
+  if (threadIdx.x == 0) {
+    counts_raw[e] = count;
+    counts_kept[e] = kept_e;
+    offsets[e] = (int32_t)off;
+    if (e == N - 1) offsets[N] = total_rows;
+    if (total_rows > R_max) report_error(status, MOE_ERR_BOUNDS, kKCapAssign, e);
+  }
+  if (total_rows > R_max) return;  // cannot happen for consistent inputs
+
+  // 2. the C-th largest score of this expert, when it overflows
+  const bool overflow = (int64_t)count > C;
+  uint32_t thr = 0u;
+  int eq_keep = INT_MAX;
+  if (overflow) {
+    uint32_t prefix = 0u, mask = 0u;
+    int need = (int)C;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = threadIdx.x; i < 256; i += kThreads) s_sel[i] = 0;
+      __syncthreads();
+      for (int64_t base = 0; base < n; base += kChunk) {
+        if (!kResident) load_items(idx, score, gate, n, base + my0, it);
+#pragma unroll
+        for (int q = 0; q < kItems; ++q)
+          if (it.ie[q] == e && (it.b[q] & mask) == prefix) atomicAdd(&s_sel[(it.b[q] >> shift) & 255u], 1);
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // the digit D holding the need-th largest: lane L owns bins 8L..8L+7;
+        // counts above each lane's bins come from a suffix scan across lanes
+        int h[8], mine = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          h[j] = s_sel[lane * 8 + j];
+          mine += h[j];
+        }
+        int suffix = mine;  // inclusive sum over lanes >= this one
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_down_sync(0xffffffffu, suffix, o);
+          if (lane + o < 32) suffix += v;
+        }
+        const int above = suffix - mine;  // requests in higher bins
+        if (above < need && need <= suffix) {
+          int run = above, D = lane * 8;
+#pragma unroll
+          for (int j = 7; j >= 0; --j) {
+            if (run + h[j] >= need) {
+              D = lane * 8 + j;
+              break;
+            }
+            run += h[j];
+          }
+          s_prefix = prefix | ((uint32_t)D << shift);
+          s_need = need - run;
+        }
+      }
+      __syncthreads();
+      prefix = s_prefix;
+      need = s_need;
+      mask |= 255u << shift;
+      __syncthreads();
+    }
+    thr = prefix;    // bit pattern of the C-th largest score
+    eq_keep = need;  // requests with exactly that score still kept, in token order
+  }
+
+  // 3. slots in token order
+  int run_eq = 0, run_kept = 0;
+  for (int64_t base = 0; base < n; base += kChunk) {
+    if (!kResident) load_items(idx, score, gate, n, base + my0, it);
+    const int64_t i0 = base + my0;
+    int my_eq = 0;
+#pragma unroll
+    for (int q = 0; q < kItems; ++q) my_eq += (it.ie[q] == e && overflow && it.b[q] == thr);
+    int tot_eq = 0;
+    int eq_rank = run_eq;
+    if (overflow) eq_rank += block_exclusive_scan(my_eq, s_warp, &tot_eq);
     bool kept[kItems];
     int my_kept = 0;
 #pragma unroll
     for (int q = 0; q < kItems; ++q) {
       bool kq = false;
-      if (ie[q] == e) {
-        if (!overflow || b[q] > thr) {
+      if (it.ie[q] == e) {
+        if (!overflow || it.b[q] > thr) {
           kq = true;
-        } else if (b[q] == thr) {
+        } else if (it.b[q] == thr) {
           kq = eq_rank < eq_keep;
           ++eq_rank;
         }
@@ -183,7 +239,7 @@ __global__ void __launch_bounds__(kThreads) cap_assign_kernel(
     int slot = block_exclusive_scan(my_kept, s_warp, &tot_kept) + run_kept;
 #pragma unroll
     for (int q = 0; q < kItems; ++q) {
-      if (ie[q] != e) continue;
+      if (it.ie[q] != e) continue;
       const int64_t i = i0 + q;
       if (kept[q] && slot >= kept_e) {  // inconsistent selection: never write past the segment
         report_error(status, MOE_ERR_BOUNDS, kKCapAssign, 2000 + e);
@@ -192,7 +248,7 @@ __global__ void __launch_bounds__(kThreads) cap_assign_kernel(
         const int64_t r = off + slot;
         row_of[i] = (int32_t)r;
         row_token[r] = (int32_t)(i / k);
-        row_gate[r] = gate[i];
+        row_gate[r] = it.g[q];
         ++slot;
       } else {
         row_of[i] = -1;
@@ -201,9 +257,9 @@ __global__ void __launch_bounds__(kThreads) cap_assign_kernel(
     run_eq += tot_eq;
     run_kept += tot_kept;
   }
-  for (int64_t r = kept_e + threadIdx.x; r < round_up_rows(kept_e); r += kThreads) {
-    row_token[off + r] = -1;
-    row_gate[off + r] = 0.f;
+  for (int64_t r = off + kept_e + threadIdx.x; r < s_end; r += kThreads) {
+    row_token[r] = -1;
+    row_gate[r] = 0.f;
   }
   if (threadIdx.x == 0 && run_kept != kept_e) report_error(status, MOE_ERR_BOUNDS, kKCapAssign, 1000 + e);
 }
@@ -214,12 +270,18 @@ cudaError_t launch_capacity(const Dims &D, const int32_t *topk_idx, const float 
                             int32_t *counts_raw, int32_t *counts_kept, int32_t *offsets, uint32_t *sel_thr,
                             int32_t *sel_eq, int32_t *row_of, int32_t *row_token, float *row_gate,
                             int32_t *status, cudaStream_t s) {
+  (void)sel_thr;
+  (void)sel_eq;
   const int64_t n = D.T * D.k;
-  cap_select_kernel<<<D.N, kThreads, 0, s>>>(topk_idx, score, n, D.C, counts_raw, counts_kept, sel_thr, sel_eq);
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  cap_assign_kernel<<<D.N, kThreads, 0, s>>>(topk_idx, gate, score, n, D.k, D.N, D.C, counts_raw, counts_kept,
-                                             sel_thr, sel_eq, offsets, row_of, row_token, row_gate, D.R_max, status);
+  const size_t smem = sizeof(int) * kWarps * D.N;
+  if (n <= (int64_t)kThreads * kItems)
+    capacity_kernel<true><<<D.N, kThreads, smem, s>>>(topk_idx, gate, score, n, D.k, D.N, D.C, counts_raw,
+                                                      counts_kept, offsets, row_of, row_token, row_gate, D.R_max,
+                                                      status);
+  else
+    capacity_kernel<false><<<D.N, kThreads, smem, s>>>(topk_idx, gate, score, n, D.k, D.N, D.C, counts_raw,
+                                                       counts_kept, offsets, row_of, row_token, row_gate, D.R_max,
+                                                       status);
   return cudaGetLastError();
 }
 

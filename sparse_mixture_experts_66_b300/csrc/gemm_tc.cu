@@ -7,24 +7,29 @@
 // scaling of the combine ("Mixture-of-Experts" wiki, step 7) is fused into the
 // second GEMM's epilogue.
 //   GEMM1: h[r, :]      = GELU(x_perm[r] . W1[e]^T + b1[e])         -> bf16
+//          (GELU via the Abramowitz & Stegun 7.1.26 erf, |error| <= 1.5e-7)
 //   GEMM2: y_perm[r, :] = row_gate[r] * (h[r] . W2[e]^T + b2[e])    -> fp32
 // for the rows r of expert e's segment. Segments start on multiples of 128
-// rows, so each 128-row tile belongs to one expert and uses one weight matrix.
+// rows, so each 128-row half tile belongs to one expert and uses one weight
+// matrix.
 //
-// One persistent CTA per SM walks the tiles of all experts (expert by expert,
-// within an expert n-tile by n-tile with the m-tiles fastest, so the expert's
-// rows stay in L2 while its weight tiles stream once). Warp roles:
-//   warp 0    TMA producer: A tile [128 x 64] and B tile [BN x 64] per stage
-//             (128-byte swizzle), ring of kStages stages;
-//   warp 1    TMEM owner and MMA issuer: one thread issues
-//             tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16) four
-//             times per stage into one of two TMEM accumulators, and commits
-//             the stage back to the producer;
-//   warps 2-9 epilogue: tcgen05.ld of the finished accumulator (warp w reads
-//             TMEM lanes 32*(w%4)...; two warps per lane quarter split the
-//             columns), bias + GELU or bias + gate scale, global stores; then
-//             the accumulator is handed back, so the epilogue of tile i
-//             overlaps the MMAs of tile i+1.
+// Persistent kernel on CTA pairs (clusters of 2, one CTA per SM): each pair
+// walks 256 x 256 output tiles of all experts (expert by expert; inside an
+// expert n-tile by n-tile with the 256-row tiles fastest, so the expert's rows
+// stay in L2 while its weight tiles stream once). Warp roles in each CTA:
+//   warp 0    TMA producer: this CTA's 128 rows of A and its half (128 rows)
+//             of the B tile per 64-deep k-block (128-byte swizzle), a ring of
+//             six 32 KB stages; completion is signalled on the leader's
+//             barrier;
+//   warp 1    TMEM owner (512 columns, allocated jointly by the pair); in the
+//             leader CTA one thread issues tcgen05.mma.cta_group::2.kind::f16
+//             (M=256, N=256, K=16) four times per stage into one of two TMEM
+//             accumulators and multicasts the commits to both CTAs;
+//   warps 2-9 epilogue: tcgen05.ld of the CTA's 128 finished rows (warp w
+//             reads TMEM lanes 32*(w%4)...; two warps per lane quarter split
+//             the columns), bias + GELU or bias + gate scale, global stores;
+//             then the accumulator is handed back to the leader, so the
+//             epilogue of tile i overlaps the MMAs of tile i+1.
 // Every wait is bounded: after kTimeoutNs the kernel records MOE_ERR_TIMEOUT,
 // all roles leave their loops, in-flight copies and MMAs are drained (bounded
 // again), TMEM is freed and the CTA exits.
@@ -43,13 +48,6 @@ constexpr int kThreads = 64 + kEpiWarps * 32;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 constexpr int kMaxExperts = 256;
 
-template <int BN> struct TileCfg {
-  static constexpr int kStages = BN == 256 ? 4 : 6;
-  static constexpr int kABytes = BM * BK * 2;
-  static constexpr int kBBytes = BN * BK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kTmemCols = 2 * BN;  // two accumulators
-};
 
 struct Ctrl {
   unsigned long long full[8], empty[8], tfull[2], tempty[2], drain;
@@ -60,9 +58,6 @@ struct Ctrl {
   int32_t tile_start[kMaxExperts + 1];
 };
 
-template <int BN> constexpr size_t smem_bytes() {
-  return 1024 + (size_t)TileCfg<BN>::kStages * TileCfg<BN>::kStageBytes + sizeof(Ctrl);
-}
 
 // ---- PTX wrappers -----------------------------------------------------------
 __device__ __forceinline__ uint32_t saddr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -114,22 +109,6 @@ __device__ __noinline__ bool mbar_wait(unsigned long long *bar, uint32_t parity,
   }
 }
 
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, unsigned long long *bar, int c0,
-                                            int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
-          saddr(dst)),
-      "l"(map), "r"(saddr(bar)), "r"(c0), "r"(c1)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, unsigned long long *bar, int c0, int c1,
-                                            int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
-      "[%2];" ::"r"(saddr(dst)),
-      "l"(map), "r"(saddr(bar)), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -147,23 +126,65 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
   return d;
 }
 
-// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
-// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
-template <int BN> __device__ __forceinline__ uint32_t idesc_bf16() {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+
+
+// ---- CTA-pair (cluster of 2) forms --------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Shared-memory address of the same variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// TMA load whose completion is signalled on an mbarrier of either CTA of the pair.
+// Wait with an inlined first probe: in steady state the phase has usually
+// completed already, and the hot MMA / producer loops skip the call.
+__device__ __forceinline__ bool mbar_wait_fast(unsigned long long *bar, uint32_t parity, volatile int *abort,
+                                               int32_t *status, int where) {
+  return mbar_try_wait(bar, parity) || mbar_wait(bar, parity, abort, status, where);
 }
 
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map, uint32_t mbar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%3, "
+      "%4}], [%2];" ::"r"(saddr(dst)),
+      "l"(map), "r"(mbar), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(void *dst, const CUtensorMap *map, uint32_t mbar, int c0, int c1,
+                                                 int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%3, "
+      "%4, %5}], [%2];" ::"r"(saddr(dst)),
+      "l"(map), "r"(mbar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
-__device__ __forceinline__ void umma_commit(unsigned long long *bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(bar))
-               : "memory");
+// Arrive (once all prior MMAs of this thread complete) on the barrier at the
+// same offset in every CTA of cta_mask.
+__device__ __forceinline__ void umma_commit_pair(unsigned long long *bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          saddr(bar)),
+      "h"(cta_mask)
+      : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -178,42 +199,59 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// ---- tile enumeration ----------------------------------------------------
-// Tiles are numbered expert by expert; inside expert e (mt_e m-tiles), tile
-// t_local = n * mt_e + m.
-__device__ __forceinline__ void decode_tile(const Ctrl *c, int N_exp, int t, int &e, int &m0, int &n_idx) {
+// ---- CTA-pair kernel --------------------------------------------------------
+// A cluster of 2 CTAs on the two SMs of a pair computes a 256 x 256 tile with
+// tcgen05.mma.cta_group::2 (M=256, N=256, K=16): each CTA stages its own 128
+// rows of A and one half (128 rows) of the B tile, so each SM moves 32 KB per
+// 64-deep k-block instead of 48 KB, and six stages fit in shared memory. The
+// leader (rank 0) issues the MMAs; D rows 0-127 land in its TMEM, rows
+// 128-255 in the peer's. Both CTAs' TMA loads signal the leader's full
+// barrier; MMA commits are multicast to both CTAs; the peer's epilogue warps
+// arrive remotely on the leader's TMEM-empty barrier.
+//
+// Tiles: per expert, pair tiles of 256 rows (two 128-row segment tiles); when
+// an expert has an odd number of 128-row tiles, the peer's half of its last
+// pair tile lies past the segment and its rows are computed but not stored.
+constexpr int kStagesP = 6;
+constexpr int kAP = BM * BK * 2;          // 16 KB: this CTA's 128 rows of A
+constexpr int kBP = 128 * BK * 2;         // 16 KB: this CTA's half of the B tile
+constexpr int kStageP = kAP + kBP;
+constexpr int BNP = 256;                  // pair tile width
+constexpr size_t kSmemP = 1024 + (size_t)kStagesP * kStageP + sizeof(Ctrl);
+
+__device__ __forceinline__ void decode_pair_tile(const Ctrl *c, int N_exp, int t, int &e, int &m0, int &n_idx) {
   int lo = 0, hi = N_exp - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (c->tile_start[mid] <= t) lo = mid; else hi = mid - 1;
   }
   e = lo;
-  const int mt = (c->offsets[e + 1] - c->offsets[e]) / BM;
+  const int mp = ((c->offsets[e + 1] - c->offsets[e]) / BM + 1) / 2;
   const int local = t - c->tile_start[e];
-  n_idx = local / mt;
-  m0 = c->offsets[e] + (local - n_idx * mt) * BM;
+  n_idx = local / mp;
+  m0 = c->offsets[e] + (local - n_idx * mp) * (2 * BM);
 }
 
-template <int BN, int EPI>
+template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                   const int32_t *__restrict__ offsets_g, int N_exp, int64_t R_max, int K, int N_out,
-                   const __nv_bfloat16 *__restrict__ bias, const float *__restrict__ row_gate, void *__restrict__ out,
-                   int32_t *status) {
-  using C = TileCfg<BN>;
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                     const int32_t *__restrict__ offsets_g, int N_exp, int64_t R_max, int K, int N_out,
+                     const __nv_bfloat16 *__restrict__ bias, const float *__restrict__ row_gate,
+                     void *__restrict__ out, int32_t *status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t *sA = base;
-  uint8_t *sB = base + C::kStages * C::kABytes;
-  Ctrl *c = (Ctrl *)(base + C::kStages * C::kStageBytes);
+  uint8_t *sB = base + kStagesP * kAP;
+  Ctrl *c = (Ctrl *)(base + kStagesP * kStageP);
   volatile int *abort = &c->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_tiles = (N_out + BN - 1) / BN;
+  const uint32_t rank = cluster_rank();
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int n_tiles = (N_out + BNP - 1) / BNP;
   const int kb_count = (K + BK - 1) / BK;
 
   if (warp == 0) {
-    // per-expert tile counts and their exclusive prefix (lane l: experts 8l..8l+7)
     int local[8];
     int sum = 0;
     bool bad = false;
@@ -224,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (e < N_exp) {
         const int o0 = offsets_g[e], o1 = offsets_g[e + 1];
         if (o1 < o0 || (o1 - o0) % BM != 0 || o1 > R_max) bad = true;
-        else local[i] = (o1 - o0) / BM * n_tiles;
+        else local[i] = ((o1 - o0) / BM + 1) / 2 * n_tiles;
       }
       sum += local[i];
     }
@@ -251,28 +289,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       c->tile_start[N_exp] = total;
       c->total_tiles = bad ? 0 : total;
       c->abort = 0;
-      if (bad) report_error(status, MOE_ERR_BOUNDS, kKGemmTc, 1);
+      if (bad && rank == 0) report_error(status, MOE_ERR_BOUNDS, kKGemmTc, 2);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      for (int s = 0; s < C::kStages; ++s) {
+      for (int s = 0; s < kStagesP; ++s) {
         mbar_init(&c->full[s], 1);
         mbar_init(&c->empty[s], 1);
       }
       for (int a = 0; a < 2; ++a) {
         mbar_init(&c->tfull[a], 1);
-        mbar_init(&c->tempty[a], kEpiWarps);
+        mbar_init(&c->tempty[a], 2 * kEpiWarps);
       }
       mbar_init(&c->drain, 1);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncwarp();
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&c->tmem_base)),
-                 "r"(C::kTmemCols));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&c->tmem_base)),
+                 "r"(2 * BNP));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // the peer's barriers are initialised before anyone signals them
   tc_fence_after();
 
   const int total = c->total_tiles;
@@ -282,31 +321,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int s = 0;
       uint32_t ph = 0;
-      uint32_t issued_parity[8];
-      bool issued[8];
-      for (int i = 0; i < 8; ++i) issued[i] = false;
+      bool issued[kStagesP];
+      uint32_t issued_parity[kStagesP];
+      for (int i = 0; i < kStagesP; ++i) issued[i] = false;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+      uint32_t full_leader[kStagesP];
+      for (int i = 0; i < kStagesP; ++i) full_leader[i] = map_to_rank(saddr(&c->full[i]), 0);
+      for (int t = pair; ok && t < total; t += npairs) {
         int e, m0, ni;
-        decode_tile(c, N_exp, t, e, m0, ni);
+        decode_pair_tile(c, N_exp, t, e, m0, ni);
+        const int a_row = m0 + (int)rank * BM, b_row = ni * BNP + (int)rank * 128;
         for (int kb = 0; kb < kb_count; ++kb) {
-          if (!mbar_wait(&c->empty[s], ph ^ 1u, abort, status, 10 + s)) {
+          if (!mbar_wait_fast(&c->empty[s], ph ^ 1u, abort, status, 50 + s)) {
             ok = false;
             break;
           }
-          mbar_expect_tx(&c->full[s], C::kStageBytes);
-          tma_load_2d(sA + s * C::kABytes, &tm_a, &c->full[s], kb * BK, m0);
-          tma_load_3d(sB + s * C::kBBytes, &tm_b, &c->full[s], kb * BK, ni * BN, e);
+          if (rank == 0) mbar_expect_tx(&c->full[s], 2 * kStageP);
+          tma_load_2d_pair(sA + s * kAP, &tm_a, full_leader[s], kb * BK, a_row);
+          tma_load_3d_pair(sB + s * kBP, &tm_b, full_leader[s], kb * BK, b_row, e);
           issued[s] = true;
           issued_parity[s] = ph;
-          if (++s == C::kStages) {
+          if (++s == kStagesP) {
             s = 0;
             ph ^= 1u;
           }
         }
       }
-      if (!ok) {  // drain the copies still in flight before the CTA frees its shared memory
-        for (int i = 0; i < C::kStages; ++i)
+      if (!ok && rank == 0) {  // the leader's full barriers track both CTAs' copies: drain them
+        for (int i = 0; i < kStagesP; ++i)
           if (issued[i]) {
             const unsigned long long t0 = globaltimer();
             while (!mbar_try_wait(&c->full[i], issued_parity[i]) && globaltimer() - t0 < kTimeoutNs) {
@@ -315,76 +357,81 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       int s = 0;
       uint32_t ph = 0, aph = 0;
       int acc = 0;
       bool ok = true, any = false;
-      const uint32_t idesc = idesc_bf16<BN>();
-      for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-        if (!mbar_wait(&c->tempty[acc], aph ^ 1u, abort, status, 20 + acc)) break;
+      const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BNP >> 3) << 17) |
+                             ((uint32_t)((2 * BM) >> 4) << 24);
+      uint64_t adesc[kStagesP], bdesc[kStagesP];
+      for (int i = 0; i < kStagesP; ++i) {
+        adesc[i] = smem_desc_sw128(saddr(sA + i * kAP));
+        bdesc[i] = smem_desc_sw128(saddr(sB + i * kBP));
+      }
+      for (int t = pair; ok && t < total; t += npairs) {
+        if (!mbar_wait_fast(&c->tempty[acc], aph ^ 1u, abort, status, 60 + acc)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
+        const uint32_t d_tmem = tmem + (uint32_t)(acc * BNP);
         for (int kb = 0; kb < kb_count; ++kb) {
-          if (!mbar_wait(&c->full[s], ph, abort, status, 30 + s)) {
+          if (!mbar_wait_fast(&c->full[s], ph, abort, status, 70 + s)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t ad = smem_desc_sw128(saddr(sA + s * C::kABytes));
-          const uint64_t bd = smem_desc_sw128(saddr(sB + s * C::kBBytes));
+          const uint64_t ad = adesc[s], bd = bdesc[s];
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
-            umma_bf16(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, (kb | kk) != 0 ? 1u : 0u);
+            umma_bf16_pair(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, (kb | kk) != 0 ? 1u : 0u);
           any = true;
-          umma_commit(&c->empty[s]);
-          if (++s == C::kStages) {
+          umma_commit_pair(&c->empty[s], (uint16_t)0x3);
+          if (++s == kStagesP) {
             s = 0;
             ph ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(&c->tfull[acc]);
+        umma_commit_pair(&c->tfull[acc], (uint16_t)0x3);
         acc ^= 1;
         if (acc == 0) aph ^= 1u;
       }
-      if (!ok || *abort) {  // wait for the MMAs already issued before TMEM is freed
-        if (any) {
-          umma_commit(&c->drain);
-          const unsigned long long t0 = globaltimer();
-          while (!mbar_try_wait(&c->drain, 0) && globaltimer() - t0 < kTimeoutNs) {
-          }
+      if ((!ok || *abort) && any) {
+        umma_commit_pair(&c->drain, (uint16_t)0x1);
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait(&c->drain, 0) && globaltimer() - t0 < kTimeoutNs) {
         }
       }
     }
   } else {
-    const int q = warp & 3;                // TMEM lane quarter this warp may read
-    const int half = (warp - 2) >> 2;      // which half of the tile's columns
-    const int row_in_tile = q * 32 + lane;
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int row_in_tile = (int)rank * BM + q * 32 + lane;
+    const uint32_t tempty_leader0 = map_to_rank(saddr(&c->tempty[0]), 0);
+    const uint32_t tempty_leader1 = map_to_rank(saddr(&c->tempty[1]), 0);
     int acc = 0;
     uint32_t aph = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    for (int t = pair; t < total; t += npairs) {
       int e, m0, ni;
-      decode_tile(c, N_exp, t, e, m0, ni);
-      // one lane waits, the warp follows its verdict: the TMEM loads below are
-      // warp-collective, so the warp must never split on a timeout
+      decode_pair_tile(c, N_exp, t, e, m0, ni);
       int ok = 0;
-      if (lane == 0) ok = mbar_wait(&c->tfull[acc], aph, abort, status, 40 + acc) ? 1 : 0;
+      if (lane == 0) ok = mbar_wait(&c->tfull[acc], aph, abort, status, 80 + acc) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
       const int64_t row = (int64_t)m0 + row_in_tile;
-      const float g = (EPI == 2 && row_gate) ? row_gate[row] : 1.0f;
+      const bool valid = row < c->offsets[e + 1];
+      const float g = (EPI == 2 && row_gate && valid) ? row_gate[row] : 1.0f;
 #pragma unroll 1
-      for (int cc = 0; cc < BN / 64; ++cc) {
-        const int col0 = half * (BN / 2) + cc * 32;
+      for (int cc = 0; cc < BNP / 64; ++cc) {
+        const int col0 = half * (BNP / 2) + cc * 32;
         uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + col0), r);
-        const int n = ni * BN + col0;
+        __syncwarp();  // the TMEM load is warp-collective: reconverge after the row-masked stores
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BNP + col0), r);
+        const int n = ni * BNP + col0;
         const __nv_bfloat16 *bp = bias + (int64_t)e * N_out + n;
 #pragma unroll
         for (int g8 = 0; g8 < 4; ++g8) {
-          if (n + g8 * 8 >= N_out) break;
+          if (!valid || n + g8 * 8 >= N_out) break;
           const uint4 braw = __ldg(reinterpret_cast<const uint4 *>(bp + g8 * 8));
           const uint32_t bw[4] = {braw.x, braw.y, braw.z, braw.w};
           float v[8];
@@ -394,14 +441,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             v[2 * j + 1] = __uint_as_float(r[g8 * 8 + 2 * j + 1]) + __uint_as_float(bw[j] & 0xffff0000u);
           }
           if (EPI == 1) {
-            uint32_t p[4];
+            uint32_t pk[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              __nv_bfloat162 h2 = __floats2bfloat162_rn(gelu_erf(v[2 * j]), gelu_erf(v[2 * j + 1]));
-              p[j] = *reinterpret_cast<uint32_t *>(&h2);
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(gelu_as(v[2 * j]), gelu_as(v[2 * j + 1]));
+              pk[j] = *reinterpret_cast<uint32_t *>(&h2);
             }
             __nv_bfloat16 *o = (__nv_bfloat16 *)out + row * N_out + n + g8 * 8;
-            *reinterpret_cast<uint4 *>(o) = make_uint4(p[0], p[1], p[2], p[3]);
+            *reinterpret_cast<uint4 *>(o) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           } else {
             float *o = (float *)out + row * N_out + n + g8 * 8;
             *reinterpret_cast<float4 *>(o) = make_float4(g * v[0], g * v[1], g * v[2], g * v[3]);
@@ -411,7 +458,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&c->tempty[acc]);
+      if (lane == 0) {
+        if (rank == 0) mbar_arrive(&c->tempty[acc]);
+        else mbar_arrive_cluster(acc == 0 ? tempty_leader0 : tempty_leader1);
+      }
       acc ^= 1;
       if (acc == 0) aph ^= 1u;
     }
@@ -419,9 +469,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // no CTA leaves while its peer may still signal its barriers
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols));
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * BNP));
   }
 }
 
@@ -464,28 +515,38 @@ int num_sms() {
   return n;
 }
 
-template <int BN, int EPI>
-cudaError_t launch_one(const Dims &D, const void *A, int64_t K, const void *B, const void *bias, int64_t N_out,
-                       const float *row_gate, const int32_t *offsets, void *out, int32_t *status, cudaStream_t s) {
+template <int EPI>
+cudaError_t launch_pair(const Dims &D, const void *A, int64_t K, const void *B, const void *bias, int64_t N_out,
+                        const float *row_gate, const int32_t *offsets, void *out, int32_t *status, cudaStream_t s) {
   static bool attr_set = false;
-  const size_t smem = smem_bytes<BN>();
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemP);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   CUtensorMap ta, tb;
   const uint64_t da[2] = {(uint64_t)K, (uint64_t)D.R_max};
   const uint64_t db[3] = {(uint64_t)K, (uint64_t)N_out, (uint64_t)D.N};
-  if (!make_map(&ta, A, 2, da, BM) || !make_map(&tb, B, 3, db, BN)) return cudaErrorInvalidValue;
-  const int64_t max_tiles = D.R_max / BM * ((N_out + BN - 1) / BN);
-  int grid = num_sms();
-  if (max_tiles < grid) grid = (int)max_tiles;
-  if (grid < 1) grid = 1;
-  gemm_tc_kernel<BN, EPI><<<grid, kThreads, smem, s>>>(ta, tb, offsets, D.N, D.R_max, (int)K, (int)N_out,
-                                                       (const __nv_bfloat16 *)bias, row_gate, out, status);
-  return cudaGetLastError();
+  if (!make_map(&ta, A, 2, da, BM) || !make_map(&tb, B, 3, db, 128)) return cudaErrorInvalidValue;
+  const int64_t max_pairs = (D.R_max / BM + D.N) / 2 * ((N_out + BNP - 1) / BNP);
+  int pairs = num_sms() / 2;
+  if (max_pairs < pairs) pairs = (int)max_pairs;
+  if (pairs < 1) pairs = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemP;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<EPI>, ta, tb, offsets, D.N, D.R_max, (int)K, (int)N_out,
+                            (const __nv_bfloat16 *)bias, row_gate, out, status);
 }
 
 }  // namespace
@@ -495,9 +556,9 @@ cudaError_t launch_ffn_tc(const Dims &D, const void *x_perm, const int32_t *offs
                           int32_t *status, cudaStream_t s) {
   if (D.dt != MOE_DT_BF16 || D.N > kMaxExperts || D.d > (1 << 30) || D.d_ff > (1 << 30))
     return cudaErrorNotSupported;
-  cudaError_t e = launch_one<256, 1>(D, x_perm, D.d, w1, b1, D.d_ff, nullptr, offsets, h, status, s);
+  cudaError_t e = launch_pair<1>(D, x_perm, D.d, w1, b1, D.d_ff, nullptr, offsets, h, status, s);
   if (e != cudaSuccess) return e;
-  return launch_one<256, 2>(D, h, D.d_ff, w2, b2, D.d, row_gate, offsets, y_perm, status, s);
+  return launch_pair<2>(D, h, D.d_ff, w2, b2, D.d, row_gate, offsets, y_perm, status, s);
 }
 
 }  // namespace moe

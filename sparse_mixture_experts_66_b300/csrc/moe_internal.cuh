@@ -49,8 +49,27 @@ template <typename T> __device__ __forceinline__ T from_f32(float v);
 template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
 
-// Exact GELU, u * Phi(u), with CUDA's erff.
+// Exact GELU, u * Phi(u), with CUDA's erff (fp32 path).
 __device__ __forceinline__ float gelu_erf(float u) { return 0.5f * u * (1.0f + erff(u * 0.70710678118654752440f)); }
+
+// GELU for the bf16 tensor-core epilogue: u * Phi(u) with erf from the
+// rational-exponential approximation of Abramowitz & Stegun, Handbook of
+// Mathematical Functions, formula 7.1.26 (Hastings):
+//   erf(z) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-z^2),
+//   t = 1 / (1 + p z), z >= 0, |error| <= 1.5e-7,
+// evaluated without branches (one reciprocal, one exp2). The result is stored
+// in bf16 (relative step 2^-8), so the approximation is invisible in h. For
+// u < 0 the complement is used directly, so tiny outputs lose no precision:
+//   GELU(u) = u (1 - q/2) for u >= 0,  u q/2 for u < 0,  q = erfc(|u|/sqrt 2).
+__device__ __forceinline__ float gelu_as(float u) {
+  const float z = fabsf(u) * 0.70710678118654752440f;
+  float t;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(fmaf(0.3275911f, z, 1.0f)));
+  const float poly =
+      t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f), -0.284496736f), 0.254829592f);
+  const float q = poly * exp2f(-z * z * 1.44269504088896341f);
+  return u >= 0.f ? u * fmaf(-0.5f, q, 1.0f) : 0.5f * u * q;
+}
 
 // The expert whose segment holds row r: offsets is non-decreasing, N+1 long.
 __device__ __forceinline__ int segment_of(const int32_t *offsets, int N, int64_t r) {

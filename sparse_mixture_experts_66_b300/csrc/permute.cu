@@ -32,7 +32,15 @@ __global__ void __launch_bounds__(kWarps * 32) permute_kernel(const uint4 *__res
     uint4 *dst = x_perm + r * vec_per_row;
     if (t >= 0 && t < T) {
       const uint4 *src = x + (int64_t)t * vec_per_row;
-      for (int64_t v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+      for (int64_t v0 = lane; v0 < vec_per_row; v0 += 32 * 4) {  // 4 loads in flight before the stores
+        uint4 tmp[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (v0 + 32 * j < vec_per_row) tmp[j] = __ldg(src + v0 + 32 * j);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (v0 + 32 * j < vec_per_row) dst[v0 + 32 * j] = tmp[j];
+      }
     } else {
       if (t >= T && lane == 0) report_error(status, MOE_ERR_BOUNDS, kKPermute, (int32_t)r);
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
@@ -91,26 +99,44 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const float *__res
     }
     const bool renorm = (flags & MOE_FLAG_RENORM_SURVIVORS) && nkept > 0;
     const bool identity = (flags & MOE_FLAG_IDENTITY_FALLBACK) && nkept == 0;
-    for (int64_t c = (int64_t)lane * 4; c < d; c += 128) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    constexpr int B = 4;  // column groups per pass: B loads per kept pick in flight
+    for (int64_t c0 = (int64_t)lane * 4; c0 < d; c0 += 128 * B) {
+      float4 acc[B];
+#pragma unroll
+      for (int b = 0; b < B; ++b) acc[b] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         if (rows[j] >= 0) {
-          const float4 v = __ldg(reinterpret_cast<const float4 *>(y_perm + (int64_t)rows[j] * d + c));
-          acc.x += v.x;
-          acc.y += v.y;
-          acc.z += v.z;
-          acc.w += v.w;
+          float4 v[B];
+          const float *src = y_perm + (int64_t)rows[j] * d;
+#pragma unroll
+          for (int b = 0; b < B; ++b)
+            if (c0 + 128 * b < d) v[b] = __ldg(reinterpret_cast<const float4 *>(src + c0 + 128 * b));
+#pragma unroll
+          for (int b = 0; b < B; ++b) {
+            if (c0 + 128 * b < d) {
+              acc[b].x += v[b].x;
+              acc[b].y += v[b].y;
+              acc[b].z += v[b].z;
+              acc[b].w += v[b].w;
+            }
+          }
         }
       }
-      if (renorm) {
-        acc.x /= kept_gate;
-        acc.y /= kept_gate;
-        acc.z /= kept_gate;
-        acc.w /= kept_gate;
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const int64_t c = c0 + 128 * b;
+        if (c >= d) continue;
+        float4 a = acc[b];
+        if (renorm) {
+          a.x /= kept_gate;
+          a.y /= kept_gate;
+          a.z /= kept_gate;
+          a.w /= kept_gate;
+        }
+        if (identity) a = Store4<T>::ld(x + t * d + c);
+        Store4<T>::st(y + t * d + c, a);
       }
-      if (identity) acc = Store4<T>::ld(x + t * d + c);
-      Store4<T>::st(y + t * d + c, acc);
     }
   }
 }

@@ -9,14 +9,16 @@
 // "Inside the Router" of "Mixture of Experts: How Sparse Routing Scales
 // Transformers" (router logits at higher precision).
 //
-// Layout of the work: a CTA of 8 warps owns 32 consecutive tokens, 4 per
-// warp. A warp streams its 4 token rows with 16-byte loads (each lane takes
-// every 32nd vector) against the rows of W_g for a chunk of 8 experts, so
-// each lane holds 4 x 8 = 32 partial dot products. One shuffle
-// reduce-scatter (31 shuffles) leaves lane L with the full logit of token
-// L/8, expert L%8 of the chunk. Logits go to shared memory; then each warp
-// reduces its tokens' softmax and top-k across lanes with shuffles (lane L
-// holds experts L, L+32, ...).
+// Layout of the work: one warp owns two tokens. Lanes stream the two token
+// rows with 16-byte loads (lane l takes every 32nd vector) against the rows of
+// W_g for a chunk of 8 experts (L1-resident), so each lane holds 2 x 8 partial
+// dot products. A shuffle reduce-scatter (offsets 16, 8, 4, 2, then a final
+// exchange at offset 1: 16 shuffles) leaves lane L with the full logit of
+// token L/16, expert (L/2)%8 of the chunk. With N <= 8 the whole softmax and
+// top-k then run in registers: the 16 lanes of a token reduce with shuffles
+// at offsets 8, 4, 2 (lanes L and L^1 hold the same value). With more experts
+// the chunk logits go to shared memory and each token is finished by the warp
+// with lane L holding experts L, L+32, ...
 #include <math.h>
 
 #include "moe_internal.cuh"
@@ -25,9 +27,10 @@ namespace moe {
 namespace {
 
 constexpr int kWarps = 8;
-constexpr int kTokPerWarp = 4;
+constexpr int kTokPerWarp = 2;
 constexpr int kTokPerBlock = kWarps * kTokPerWarp;
-constexpr int kEC = 8;  // experts per chunk: kTokPerWarp * kEC = 32 partial sums per lane
+constexpr int kEC = 8;  // experts per chunk
+constexpr size_t kMaxStagedW = 96 * 1024;  // W_g bytes staged in shared memory per CTA
 constexpr unsigned kFull = 0xffffffffu;
 
 template <typename T> struct VecN;
@@ -48,69 +51,186 @@ __device__ __forceinline__ void load16(const __nv_bfloat16 *p, float (&v)[8]) {
   }
 }
 
-// 32 values per lane -> lane L returns the warp-wide sum of value L.
-__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
+// W_g rows may live in shared memory (staged) or global memory: generic loads.
+__device__ __forceinline__ void load16w(const float *p, float (&v)[4]) {
+  float4 q = *reinterpret_cast<const float4 *>(p);
+  v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+}
+__device__ __forceinline__ void load16w(const __nv_bfloat16 *p, float (&v)[8]) {
+  uint4 q = *reinterpret_cast<const uint4 *>(p);
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-  for (int half = 16; half >= 1; half >>= 1) {
-    const bool up = (lane & half) != 0;
-#pragma unroll
-    for (int i = 0; i < half; ++i) {
-      float send = up ? v[i] : v[i + half];
-      float keep = up ? v[i + half] : v[i];
-      v[i] = keep + __shfl_xor_sync(kFull, send, half);
-    }
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
   }
-  return v[0];
 }
 
+// 16 values per lane -> lane L returns the warp-wide sum of value (L >> 1) & 15.
+__device__ __forceinline__ float reduce_scatter16(float (&v)[16], int lane) {
+#pragma unroll
+  for (int n = 16, off = 16; n >= 2; n >>= 1, off >>= 1) {
+    const bool up = (lane & off) != 0;
+    const int h = n >> 1;
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+      const float send = up ? v[i] : v[i + h];
+      const float keep = up ? v[i + h] : v[i];
+      v[i] = keep + __shfl_xor_sync(kFull, send, off);
+    }
+  }
+  return v[0] + __shfl_xor_sync(kFull, v[0], 1);
+}
+
+// Partial logits of 2 tokens x 8 experts (e0 .. e0+7) for this lane's slice.
+// Each pass first issues the loads of kBatch vectors of both token rows (so
+// that many bytes are in flight per lane), then walks the expert rows (L1).
+constexpr int kBatch = 4;
+template <typename T>
+__device__ __forceinline__ void chunk_logits(const T *__restrict__ x0, const T *__restrict__ x1, bool has1,
+                                             const T *__restrict__ w_g, int d, int N, int e0, int lane,
+                                             float (&acc)[16]) {
+  constexpr int V = VecN<T>::n;
+  const int nvec = d / V;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  for (int vb = lane; vb < nvec; vb += 32 * kBatch) {
+    float xa[kBatch][V], xb[kBatch][V];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int v = vb + 32 * j;
+      if (v < nvec) {
+        load16(x0 + (int64_t)v * V, xa[j]);
+        if (has1) {
+          load16(x1 + (int64_t)v * V, xb[j]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < V; ++q) xb[j][q] = 0.f;
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < V; ++q) xa[j][q] = xb[j][q] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < kEC; ++e) {
+      if (e0 + e < N) {
+        const T *wr = w_g + (int64_t)(e0 + e) * d;
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+          const int v = vb + 32 * j;
+          if (v < nvec) {
+            float wv[V];
+            load16w(wr + (int64_t)v * V, wv);
+#pragma unroll
+            for (int q = 0; q < V; ++q) {
+              acc[e] = fmaf(xa[j][q], wv[q], acc[e]);
+              acc[8 + e] = fmaf(xb[j][q], wv[q], acc[8 + e]);
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
+// N <= 8: everything in registers. W_g is staged in shared memory by one
+// cooperative load per CTA (when it fits), so the projection reads it at
+// shared-memory latency instead of a chain of cache misses.
+template <typename T, bool kStageW>
+__global__ void __launch_bounds__(kWarps * 32) router_small_kernel(const T *__restrict__ x, const T *__restrict__ w_g,
+                                                                   const float *__restrict__ router_bias, int64_t T_,
+                                                                   int d, int N, int k, int32_t *__restrict__ topk_idx,
+                                                                   float *__restrict__ gate,
+                                                                   float *__restrict__ score) {
+  extern __shared__ uint4 s_w[];  // [N * d * sizeof(T) / 16]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const T *w = w_g;
+  if (kStageW) {
+    const int nv = N * d * (int)sizeof(T) / 16;
+    const uint4 *src = reinterpret_cast<const uint4 *>(w_g);
+    for (int i = threadIdx.x; i < nv; i += kWarps * 32) s_w[i] = __ldg(src + i);
+    __syncthreads();
+    w = reinterpret_cast<const T *>(s_w);
+  }
+  const int64_t t0 = ((int64_t)blockIdx.x * kWarps + warp) * kTokPerWarp;
+  if (t0 >= T_) return;
+  const bool has1 = t0 + 1 < T_;
+  float acc[16];
+  chunk_logits(x + t0 * d, x + (t0 + 1) * d, has1, w, d, N, 0, lane, acc);
+  float l = reduce_scatter16(acc, lane);
+  const int e = (lane >> 1) & 7;
+  const int64_t t = t0 + (lane >> 4);
+  const bool valid = e < N;
+  if (valid && router_bias) l += router_bias[e];
+  if (!valid) l = -INFINITY;
+  float m = l;
+#pragma unroll
+  for (int off = 8; off >= 2; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+  const float ex = valid ? expf(l - m) : 0.f;
+  float s = ex;
+#pragma unroll
+  for (int off = 8; off >= 2; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
+  bool taken = !valid;
+  float sel_ex[8];
+  int sel_e[8];
+  float sel_sum = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j < k) {
+      float bv = taken ? -INFINITY : l;
+      int be = taken ? 0x7fffffff : e;
+#pragma unroll
+      for (int off = 8; off >= 2; off >>= 1) {
+        const float ov = __shfl_xor_sync(kFull, bv, off);
+        const int oe = __shfl_xor_sync(kFull, be, off);
+        if (ov > bv || (ov == bv && oe < be)) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      if (be == e) taken = true;
+      sel_e[j] = be;
+      sel_ex[j] = expf(bv - m);
+      sel_sum += sel_ex[j];
+    }
+  }
+  if ((lane & 15) == 0 && t < T_) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < k) {
+        topk_idx[t * k + j] = sel_e[j];
+        score[t * k + j] = sel_ex[j] / s;
+        gate[t * k + j] = sel_ex[j] / sel_sum;
+      }
+    }
+  }
+}
+
+// Any N <= 256: chunk logits through shared memory.
 template <typename T>
 __global__ void __launch_bounds__(kWarps * 32) router_kernel(const T *__restrict__ x, const T *__restrict__ w_g,
                                                              const float *__restrict__ router_bias, int64_t T_,
                                                              int d, int N, int k, int32_t *__restrict__ topk_idx,
                                                              float *__restrict__ gate, float *__restrict__ score) {
   extern __shared__ float s_logits[];  // [kTokPerBlock][N]
-  constexpr int V = VecN<T>::n;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t tok0 = (int64_t)blockIdx.x * kTokPerBlock + warp * kTokPerWarp;
-  const int nvec = d / V;
-
+  const int64_t t0 = ((int64_t)blockIdx.x * kWarps + warp) * kTokPerWarp;
+  if (t0 >= T_) return;
+  const bool has1 = t0 + 1 < T_;
+  float *my = s_logits + warp * kTokPerWarp * N;
   for (int e0 = 0; e0 < N; e0 += kEC) {
-    float acc[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-    for (int v = lane; v < nvec; v += 32) {
-      float xv[kTokPerWarp][V];
-#pragma unroll
-      for (int tk = 0; tk < kTokPerWarp; ++tk) {
-        if (tok0 + tk < T_) {
-          load16(x + (tok0 + tk) * (int64_t)d + (int64_t)v * V, xv[tk]);
-        } else {
-#pragma unroll
-          for (int q = 0; q < V; ++q) xv[tk][q] = 0.f;
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < kEC; ++e) {
-        if (e0 + e < N) {
-          float wv[V];
-          load16(w_g + (int64_t)(e0 + e) * d + (int64_t)v * V, wv);
-#pragma unroll
-          for (int tk = 0; tk < kTokPerWarp; ++tk)
-#pragma unroll
-            for (int q = 0; q < V; ++q) acc[tk * kEC + e] = fmaf(xv[tk][q], wv[q], acc[tk * kEC + e]);
-        }
-      }
-    }
-    const float r = reduce_scatter32(acc, lane);
-    const int tk = lane >> 3, e = e0 + (lane & 7);
-    if (e < N) s_logits[(warp * kTokPerWarp + tk) * N + e] = r;
+    float acc[16];
+    chunk_logits(x + t0 * d, x + (t0 + 1) * d, has1, w_g, d, N, e0, lane, acc);
+    const float r = reduce_scatter16(acc, lane);
+    const int e = e0 + ((lane >> 1) & 7);
+    if ((lane & 1) == 0 && e < N) my[(lane >> 4) * N + e] = r;
   }
   __syncwarp();
-
   for (int tk = 0; tk < kTokPerWarp; ++tk) {
-    const int64_t t = tok0 + tk;
+    const int64_t t = t0 + tk;
     if (t >= T_) break;
-    const float *L = s_logits + (warp * kTokPerWarp + tk) * N;
+    const float *L = my + tk * N;
     float lv[8];
     float m = -INFINITY;
 #pragma unroll
@@ -131,7 +251,6 @@ __global__ void __launch_bounds__(kWarps * 32) router_kernel(const T *__restrict
       if (lane + 32 * i < N) s += expf(lv[i] - m);
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
-
     uint32_t taken = 0;
     float sel_ex[8];
     int sel_e[8];
@@ -183,14 +302,31 @@ cudaError_t launch_router(const Dims &D, const void *x, const void *w_g, const f
                           int32_t *topk_idx, float *gate, float *score, int32_t *status, cudaStream_t s) {
   (void)status;
   const unsigned grid = (unsigned)((D.T + kTokPerBlock - 1) / kTokPerBlock);
-  const size_t smem = sizeof(float) * kTokPerBlock * D.N;
-  if (D.dt == MOE_DT_BF16) {
-    router_kernel<__nv_bfloat16><<<grid, kWarps * 32, smem, s>>>(
-        (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)w_g, router_bias, D.T, (int)D.d, D.N, D.k, topk_idx,
-        gate, score);
+  const bool bf16 = D.dt == MOE_DT_BF16;
+  if (D.N <= kEC) {
+    const size_t wbytes = (size_t)D.N * D.d * (bf16 ? 2 : 4);
+    const bool stage = wbytes <= kMaxStagedW;
+    const size_t smem = stage ? wbytes : 0;
+    if (bf16) {
+      auto kern = stage ? router_small_kernel<__nv_bfloat16, true> : router_small_kernel<__nv_bfloat16, false>;
+      if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      kern<<<grid, kWarps * 32, smem, s>>>((const __nv_bfloat16 *)x, (const __nv_bfloat16 *)w_g, router_bias, D.T,
+                                           (int)D.d, D.N, D.k, topk_idx, gate, score);
+    } else {
+      auto kern = stage ? router_small_kernel<float, true> : router_small_kernel<float, false>;
+      if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      kern<<<grid, kWarps * 32, smem, s>>>((const float *)x, (const float *)w_g, router_bias, D.T, (int)D.d, D.N,
+                                           D.k, topk_idx, gate, score);
+    }
   } else {
-    router_kernel<float><<<grid, kWarps * 32, smem, s>>>((const float *)x, (const float *)w_g, router_bias, D.T,
-                                                         (int)D.d, D.N, D.k, topk_idx, gate, score);
+    const size_t smem = sizeof(float) * kTokPerBlock * D.N;
+    if (bf16)
+      router_kernel<__nv_bfloat16><<<grid, kWarps * 32, smem, s>>>((const __nv_bfloat16 *)x,
+                                                                   (const __nv_bfloat16 *)w_g, router_bias, D.T,
+                                                                   (int)D.d, D.N, D.k, topk_idx, gate, score);
+    else
+      router_kernel<float><<<grid, kWarps * 32, smem, s>>>((const float *)x, (const float *)w_g, router_bias, D.T,
+                                                           (int)D.d, D.N, D.k, topk_idx, gate, score);
   }
   return cudaGetLastError();
 }

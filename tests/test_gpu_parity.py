@@ -105,6 +105,30 @@ def test_expert_ffn_rows_against_oracle(w):
     assert max(errs) <= parity.TOL[w.dtype] * max(scale)
 
 
+@pytest.mark.parametrize("w", [STAGE_CASES[0], WORKLOADS[HEADLINE]], ids=lambda w: w.name)
+def test_hidden_activations_within_bf16_rounding_of_exact_gelu(w):
+    """h = GELU(x_perm W1^T + b1) from the first GEMM's epilogue equals the
+    exact (erf) GELU of the oracle up to the bf16 rounding of h and the fp32
+    accumulation error: |h - h_ref| <= 2^-8 |h_ref| + 1e-4."""
+    inp = draw(w)
+    g = parity.run_gpu(w, inp)
+    v = g["_ws"].views()
+    xp = v["x_perm"].float().cpu().numpy()
+    hh = v["h"].float().cpu().numpy()
+    off = g["offsets"]
+    w1, b1, w2, b2 = (as_f32_numpy(inp[n]) for n in ("w1", "b1", "w2", "b2"))
+    rng = np.random.default_rng(1)
+    orc = O.load()
+    rows = [r for r in rng.choice(int(off[-1]), size=64, replace=False) if g["row_token"][r] >= 0]
+    worst = 0.0
+    for r in rows:
+        e = int(np.searchsorted(off, r, side="right") - 1)
+        h_ref, _ = orc.expert_ffn_hidden(xp[r], w1[e], b1[e], w2[e], b2[e])
+        excess = np.abs(hh[r] - h_ref) - (2.0 ** -8 * np.abs(h_ref) + 1e-4)
+        worst = max(worst, float(excess.max()))
+    assert worst <= 0.0, worst
+
+
 def test_router_against_oracle():
     w = custom(2048, 1024, 64, 8, 2, math.inf, seed=5)
     inp = draw(w)
