@@ -88,8 +88,9 @@ typedef struct {
 
 /* Byte offsets of the buffers inside a workspace (all 256-byte aligned).
  * rows = R_max, the row capacity of the permuted buffers: every expert segment
- * starts on a multiple of 128 rows, so R_max = floor((min(T*k, N*C) +
- * 127*N) / 128) * 128. */
+ * starts on a multiple of 128 rows (64 rows for decode-shaped configs: bf16
+ * with T*k <= 64*N), so R_max = floor((min(T*k, N*C) + 127*N) / 128) * 128
+ * bounds the rows in use. */
 typedef struct {
   size_t status;      /* int32[16]; [0] first device error code, [1] kernel id, [2] detail */
   size_t topk_idx;    /* int32 [T, k]  picks in rank order */
@@ -106,6 +107,7 @@ typedef struct {
   size_t x_perm;      /* dtype [rows, d]    tokens gathered per expert */
   size_t h;           /* dtype [rows, d_ff] expert hidden activations */
   size_t y_perm;      /* fp32  [rows, d]    gate-scaled expert outputs */
+  size_t y_split;     /* fp32  [S-1, rows, d] decode-shaped configs only: the second GEMM's extra K slices */
   size_t total;       /* bytes of the whole workspace */
   int64_t rows;       /* R_max */
   int64_t capacity;   /* C */
@@ -168,7 +170,10 @@ moe_status moe_dispatch(const moe_config *cfg, const void *x, const int32_t *top
  * for every row r of expert e's segment [offsets[e], offsets[e+1]).
  *   row_gate may be NULL (no scaling). h [rows, d_ff] may be NULL to use the
  *   workspace's h buffer. Accumulation is fp32 (bf16 inputs: tensor cores,
- *   tcgen05, accumulating in tensor memory). */
+ *   tcgen05, accumulating in tensor memory). For decode-shaped configs (bf16,
+ *   T*k <= 64*N) the second GEMM is split along d_ff: y_perm receives the
+ *   first slice and the workspace's y_split the others, which moe_combine
+ *   (given the same workspace) adds in slice order. */
 moe_status moe_expert_ffn(const moe_config *cfg, const void *x_perm, const int32_t *offsets, const void *w1,
                           const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
                           float *y_perm, void *ws, moe_stream_t stream);

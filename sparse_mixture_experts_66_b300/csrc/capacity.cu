@@ -11,7 +11,8 @@
 //   1. every CTA counts the requests of all N experts (warp-aggregated with
 //      match_any into per-warp rows of a shared histogram), so each CTA can
 //      compute every segment offset itself: offset[e] = sum over e' < e of
-//      roundup(min(count[e'], C), 128). No CTA waits for another;
+//      roundup(min(count[e'], C), A), A = 128 rows (64 for decode-shaped
+//      batches). No CTA waits for another;
 //   2. if its expert overflows, the CTA radix-selects (4 passes of 8 bits over
 //      the fp32 score's bit pattern, which orders non-negative floats) the C-th
 //      largest score and how many requests equal to it are still kept;
@@ -29,7 +30,7 @@ constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kItems = 8;  // consecutive requests per thread
 
-__device__ __forceinline__ int64_t round_up_rows(int64_t v) { return (v + kRowAlign - 1) / kRowAlign * kRowAlign; }
+__device__ __forceinline__ int64_t round_up_rows(int64_t v, int align) { return (v + align - 1) / align * align; }
 
 // Exclusive scan over the block in thread order; *total gets the block sum.
 __device__ __forceinline__ int block_exclusive_scan(int v, int *s_warp, int *total) {
@@ -96,8 +97,8 @@ __device__ __forceinline__ void load_items(const int32_t *__restrict__ idx, cons
 template <bool kResident>
 __global__ void __launch_bounds__(kThreads) capacity_kernel(
     const int32_t *__restrict__ idx, const float *__restrict__ gate, const float *__restrict__ score, int64_t n,
-    int k, int N, int64_t C, int32_t *counts_raw, int32_t *counts_kept, int32_t *offsets, int32_t *row_of,
-    int32_t *row_token, float *row_gate, int64_t R_max, int32_t *status) {
+    int k, int N, int64_t C, int align, int32_t *counts_raw, int32_t *counts_kept, int32_t *offsets,
+    int32_t *row_of, int32_t *row_token, float *row_gate, int64_t R_max, int32_t *status) {
   extern __shared__ int s_hist[];  // [kWarps][N]
   __shared__ int s_warp[32];
   __shared__ int s_sel[256];
@@ -129,7 +130,7 @@ __global__ void __launch_bounds__(kThreads) capacity_kernel(
   int padded = 0, cnt = 0;
   if (threadIdx.x < N) {
     for (int w = 0; w < kWarps; ++w) cnt += s_hist[w * N + threadIdx.x];
-    padded = (int)round_up_rows(cnt < C ? cnt : C);
+    padded = (int)round_up_rows(cnt < C ? cnt : C, align);
   }
   int total_rows;
   const int excl = block_exclusive_scan(padded, s_warp, &total_rows);
@@ -275,13 +276,13 @@ cudaError_t launch_capacity(const Dims &D, const int32_t *topk_idx, const float 
   const int64_t n = D.T * D.k;
   const size_t smem = sizeof(int) * kWarps * D.N;
   if (n <= (int64_t)kThreads * kItems)
-    capacity_kernel<true><<<D.N, kThreads, smem, s>>>(topk_idx, gate, score, n, D.k, D.N, D.C, counts_raw,
-                                                      counts_kept, offsets, row_of, row_token, row_gate, D.R_max,
-                                                      status);
+    capacity_kernel<true><<<D.N, kThreads, smem, s>>>(topk_idx, gate, score, n, D.k, D.N, D.C, row_align(D),
+                                                      counts_raw, counts_kept, offsets, row_of, row_token, row_gate,
+                                                      D.R_max, status);
   else
-    capacity_kernel<false><<<D.N, kThreads, smem, s>>>(topk_idx, gate, score, n, D.k, D.N, D.C, counts_raw,
-                                                       counts_kept, offsets, row_of, row_token, row_gate, D.R_max,
-                                                       status);
+    capacity_kernel<false><<<D.N, kThreads, smem, s>>>(topk_idx, gate, score, n, D.k, D.N, D.C, row_align(D),
+                                                       counts_raw, counts_kept, offsets, row_of, row_token, row_gate,
+                                                       D.R_max, status);
   return cudaGetLastError();
 }
 

@@ -33,19 +33,17 @@
 // Every wait is bounded: after kTimeoutNs the kernel records MOE_ERR_TIMEOUT,
 // all roles leave their loops, in-flight copies and MMAs are drained (bounded
 // again), TMEM is freed and the CTA exits.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include "moe_internal.cuh"
+#include "tc_common.cuh"
 
 namespace moe {
 namespace {
+
+using namespace tc;
 
 constexpr int BM = 128;
 constexpr int BK = 64;  // one 128-byte swizzle atom of bf16
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + kEpiWarps * 32;
-constexpr unsigned long long kTimeoutNs = 2000000000ull;
 constexpr int kMaxExperts = 256;
 
 
@@ -57,75 +55,6 @@ struct Ctrl {
   int32_t offsets[kMaxExperts + 1];
   int32_t tile_start[kMaxExperts + 1];
 };
-
-
-// ---- PTX wrappers -----------------------------------------------------------
-__device__ __forceinline__ uint32_t saddr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ unsigned long long globaltimer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(unsigned long long *bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(bar)), "r"(count));
-}
-__device__ __forceinline__ void mbar_expect_tx(unsigned long long *bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(bar)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(unsigned long long *bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(unsigned long long *bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(saddr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait for the phase of the given parity. Returns false (and raises
-// the CTA's abort flag, recording MOE_ERR_TIMEOUT once) when the limit passes,
-// or when another role has aborted.
-__device__ __noinline__ bool mbar_wait(unsigned long long *bar, uint32_t parity, volatile int *abort,
-                                       int32_t *status, int where) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0) {
-      if (*abort) return false;
-      if (globaltimer() - t0 > kTimeoutNs) {
-        report_error(status, MOE_ERR_TIMEOUT, kKGemmTc, where);
-        *abort = 1;
-        return false;
-      }
-    }
-  }
-}
-
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// K-major operand tile with 128-byte swizzle: rows of 128 bytes, 8-row atoms
-// of 1024 bytes (the stride-dimension byte offset); the leading offset is
-// unused for this layout. Bits 46-47 hold the descriptor version (1).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)1 << 16;
-  d |= (uint64_t)(1024 >> 4) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
-
 
 
 // ---- CTA-pair (cluster of 2) forms --------------------------------------
@@ -147,12 +76,6 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 // TMA load whose completion is signalled on an mbarrier of either CTA of the pair.
-// Wait with an inlined first probe: in steady state the phase has usually
-// completed already, and the hot MMA / producer loops skip the call.
-__device__ __forceinline__ bool mbar_wait_fast(unsigned long long *bar, uint32_t parity, volatile int *abort,
-                                               int32_t *status, int where) {
-  return mbar_try_wait(bar, parity) || mbar_wait(bar, parity, abort, status, where);
-}
 
 __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map, uint32_t mbar, int c0, int c1) {
   asm volatile(
@@ -187,17 +110,6 @@ __device__ __forceinline__ void umma_commit_pair(unsigned long long *bar, uint16
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
 
 // ---- CTA-pair kernel --------------------------------------------------------
 // A cluster of 2 CTAs on the two SMs of a pair computes a 256 x 256 tile with
@@ -332,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         decode_pair_tile(c, N_exp, t, e, m0, ni);
         const int a_row = m0 + (int)rank * BM, b_row = ni * BNP + (int)rank * 128;
         for (int kb = 0; kb < kb_count; ++kb) {
-          if (!mbar_wait_fast(&c->empty[s], ph ^ 1u, abort, status, 50 + s)) {
+          if (!mbar_wait_fast(&c->empty[s], ph ^ 1u, abort, status, kKGemmTc, 50 + s)) {
             ok = false;
             break;
           }
@@ -370,11 +282,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         bdesc[i] = smem_desc_sw128(saddr(sB + i * kBP));
       }
       for (int t = pair; ok && t < total; t += npairs) {
-        if (!mbar_wait_fast(&c->tempty[acc], aph ^ 1u, abort, status, 60 + acc)) break;
+        if (!mbar_wait_fast(&c->tempty[acc], aph ^ 1u, abort, status, kKGemmTc, 60 + acc)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + (uint32_t)(acc * BNP);
         for (int kb = 0; kb < kb_count; ++kb) {
-          if (!mbar_wait_fast(&c->full[s], ph, abort, status, 70 + s)) {
+          if (!mbar_wait_fast(&c->full[s], ph, abort, status, kKGemmTc, 70 + s)) {
             ok = false;
             break;
           }
@@ -414,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int e, m0, ni;
       decode_pair_tile(c, N_exp, t, e, m0, ni);
       int ok = 0;
-      if (lane == 0) ok = mbar_wait(&c->tfull[acc], aph, abort, status, 80 + acc) ? 1 : 0;
+      if (lane == 0) ok = mbar_wait(&c->tfull[acc], aph, abort, status, kKGemmTc, 80 + acc) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
@@ -474,45 +386,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * BNP));
   }
-}
-
-// ---- host side ------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
-  }
-  return fn;
-}
-
-// bf16 tensor [outer..., inner] with a box of {64, box_rows(, 1)} and 128-byte swizzle.
-bool make_map(CUtensorMap *m, const void *ptr, int rank, const uint64_t *dims, uint32_t box_rows) {
-  auto enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t gd[3], gs[2];
-  cuuint32_t box[3] = {(cuuint32_t)BK, box_rows, 1}, es[3] = {1, 1, 1};
-  for (int i = 0; i < rank; ++i) gd[i] = dims[i];
-  gs[0] = dims[0] * 2;
-  if (rank == 3) gs[1] = dims[0] * dims[1] * 2;
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(ptr), gd, gs, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-int num_sms() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
 }
 
 template <int EPI>

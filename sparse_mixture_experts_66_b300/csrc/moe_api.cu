@@ -92,6 +92,8 @@ void make_layout(const Dims &D, moe_workspace_layout *L) {
   L->x_perm = take(R * (size_t)D.d * es);
   L->h = take(R * (size_t)D.d_ff * es);
   L->y_perm = take(R * (size_t)D.d * 4);
+  const int S = decode_splits(D);
+  L->y_split = take(S > 1 ? (size_t)(S - 1) * R * (size_t)D.d * 4 : 0);
   L->total = off;
   L->rows = D.R_max;
   L->capacity = D.C;
@@ -121,7 +123,9 @@ moe_status check_opt(const void *p, const char *what) {
 moe_status do_route(const Dims &D, const moe_workspace_layout &L, const void *x, const void *w_g,
                     const float *router_bias, int32_t *topk_idx, float *gate, float *score, void *ws,
                     cudaStream_t s) {
-  cudaError_t e = launch_router(D, x, w_g, router_bias, topk_idx, gate, score, AT(ws, L.status, int32_t *), s);
+  cudaError_t e = D.dt == MOE_DT_BF16
+                      ? launch_router_tc(D, x, w_g, router_bias, topk_idx, gate, score, AT(ws, L.status, int32_t *), s)
+                      : launch_router(D, x, w_g, router_bias, topk_idx, gate, score, AT(ws, L.status, int32_t *), s);
   if (e != cudaSuccess) return cuda_fail(e, "router launch");
   return MOE_OK;
 }
@@ -144,6 +148,14 @@ moe_status do_ffn(const Dims &D, const moe_workspace_layout &L, const void *x_pe
                   const void *w1, const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
                   float *y_perm, void *ws, cudaStream_t s) {
   int32_t *status = AT(ws, L.status, int32_t *);
+  if (decode_splits(D) > 0) {
+    cudaError_t e = launch_ffn_decode(D, x_perm, offsets, w1, b1, w2, b2, row_gate, h, y_perm,
+                                      AT(ws, L.y_split, float *), status, s);
+    if (e == cudaErrorNotSupported)
+      return fail(MOE_ERR_UNSUPPORTED, "expert FFN: decode shape not supported by the tensor-core kernels");
+    if (e != cudaSuccess) return cuda_fail(e, "expert FFN (decode, tensor cores)");
+    return MOE_OK;
+  }
   if (D.dt == MOE_DT_BF16) {
     cudaError_t e = launch_ffn_tc(D, x_perm, offsets, w1, b1, w2, b2, row_gate, h, y_perm, status, s);
     if (e == cudaErrorNotSupported)
@@ -160,7 +172,9 @@ moe_status do_ffn(const Dims &D, const moe_workspace_layout &L, const void *x_pe
 
 moe_status do_combine(const Dims &D, const moe_workspace_layout &L, const float *y_perm, const int32_t *row_of,
                       const float *gate, const void *x, void *y, void *ws, cudaStream_t s) {
-  cudaError_t e = launch_combine(D, y_perm, row_of, gate, x, y, AT(ws, L.status, int32_t *), s);
+  const int S = decode_splits(D);
+  cudaError_t e = launch_combine(D, y_perm, S > 1 ? AT(ws, L.y_split, const float *) : nullptr, S > 1 ? S - 1 : 0,
+                                 row_of, gate, x, y, AT(ws, L.status, int32_t *), s);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   return MOE_OK;
 }

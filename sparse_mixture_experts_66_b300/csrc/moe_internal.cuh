@@ -12,6 +12,10 @@ namespace moe {
 // Every expert segment of the permuted buffers starts on a multiple of this
 // many rows, so that a 128-row GEMM tile never spans two experts.
 constexpr int kRowAlign = 128;
+// Decode-shaped batches (at most this many expected rows per expert,
+// T*k <= 64*N) run the swap-AB expert GEMMs, whose token chunks are 64 rows:
+// their segments start on multiples of 64 rows instead.
+constexpr int kDecodeRowsPerExpert = 64;
 
 // Kernel ids recorded next to a device error code in the status word.
 enum KernelId : int32_t {
@@ -88,16 +92,35 @@ void set_last_error(const char *text);
 cudaError_t launch_router(const Dims &D, const void *x, const void *w_g, const float *router_bias,
                           int32_t *topk_idx, float *gate, float *score, int32_t *status, cudaStream_t s);
 
+// Router on the tensor cores (bf16 inputs, N <= 256); cudaErrorNotSupported otherwise.
+cudaError_t launch_router_tc(const Dims &D, const void *x, const void *w_g, const float *router_bias,
+                             int32_t *topk_idx, float *gate, float *score, int32_t *status, cudaStream_t s);
+
 cudaError_t launch_capacity(const Dims &D, const int32_t *topk_idx, const float *gate, const float *score,
                             int32_t *counts_raw, int32_t *counts_kept, int32_t *offsets, uint32_t *sel_thr,
                             int32_t *sel_eq, int32_t *row_of, int32_t *row_token, float *row_gate,
                             int32_t *status, cudaStream_t s);
 
+// Number of K slices of the decode-mode second GEMM (>= 1), or 0 when the
+// config is not decode-shaped (bf16 and T*k <= 64*N).
+int decode_splits(const Dims &D);
+// Segment alignment of the permuted buffers for this config.
+inline int row_align(const Dims &D) { return decode_splits(D) > 0 ? kDecodeRowsPerExpert : kRowAlign; }
+
+// Swap-AB expert FFNs for decode-shaped batches. y_split holds the second
+// GEMM's K slices 1..S-1 (S = decode_splits), each [R_max, d] fp32.
+cudaError_t launch_ffn_decode(const Dims &D, const void *x_perm, const int32_t *offsets, const void *w1,
+                              const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
+                              float *y_perm, float *y_split, int32_t *status, cudaStream_t s);
+
 cudaError_t launch_permute(const Dims &D, const void *x, const int32_t *offsets, const int32_t *row_token,
                            void *x_perm, int32_t *status, cudaStream_t s);
 
-cudaError_t launch_combine(const Dims &D, const float *y_perm, const int32_t *row_of, const float *gate,
-                           const void *x, void *y, int32_t *status, cudaStream_t s);
+// y_split / nsplit: the extra K slices of a decode-mode second GEMM (nsplit
+// buffers of [R_max, d] after y_perm's own), added in slice order.
+cudaError_t launch_combine(const Dims &D, const float *y_perm, const float *y_split, int nsplit,
+                           const int32_t *row_of, const float *gate, const void *x, void *y, int32_t *status,
+                           cudaStream_t s);
 
 // Grouped GEMM over expert segments with the two fused epilogues.
 //   epi 1: out[r, n] = GELU(A[r] . B[e, n] + bias[e, n])            (dtype)

@@ -70,7 +70,9 @@ template <> struct Store4<__nv_bfloat16> {
 };
 
 template <typename T>
-__global__ void __launch_bounds__(kWarps * 32) combine_kernel(const float *__restrict__ y_perm, int64_t d,
+__global__ void __launch_bounds__(kWarps * 32) combine_kernel(const float *__restrict__ y_perm,
+                                                              const float *__restrict__ y_split, int nsplit,
+                                                              int64_t d,
                                                               const int32_t *__restrict__ row_of,
                                                               const float *__restrict__ gate,
                                                               const T *__restrict__ x, int64_t T_, int k,
@@ -107,18 +109,21 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const float *__res
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         if (rows[j] >= 0) {
-          float4 v[B];
-          const float *src = y_perm + (int64_t)rows[j] * d;
+          // the pick's row: y_perm, then the K slices of a decode-mode GEMM in order
+          for (int sl = 0; sl <= nsplit; ++sl) {
+            float4 v[B];
+            const float *src = (sl == 0 ? y_perm : y_split + (int64_t)(sl - 1) * R_max * d) + (int64_t)rows[j] * d;
 #pragma unroll
-          for (int b = 0; b < B; ++b)
-            if (c0 + 128 * b < d) v[b] = __ldg(reinterpret_cast<const float4 *>(src + c0 + 128 * b));
+            for (int b = 0; b < B; ++b)
+              if (c0 + 128 * b < d) v[b] = __ldg(reinterpret_cast<const float4 *>(src + c0 + 128 * b));
 #pragma unroll
-          for (int b = 0; b < B; ++b) {
-            if (c0 + 128 * b < d) {
-              acc[b].x += v[b].x;
-              acc[b].y += v[b].y;
-              acc[b].z += v[b].z;
-              acc[b].w += v[b].w;
+            for (int b = 0; b < B; ++b) {
+              if (c0 + 128 * b < d) {
+                acc[b].x += v[b].x;
+                acc[b].y += v[b].y;
+                acc[b].z += v[b].z;
+                acc[b].w += v[b].w;
+              }
             }
           }
         }
@@ -160,15 +165,18 @@ cudaError_t launch_permute(const Dims &D, const void *x, const int32_t *offsets,
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const Dims &D, const float *y_perm, const int32_t *row_of, const float *gate,
-                           const void *x, void *y, int32_t *status, cudaStream_t s) {
+cudaError_t launch_combine(const Dims &D, const float *y_perm, const float *y_split, int nsplit,
+                           const int32_t *row_of, const float *gate, const void *x, void *y, int32_t *status,
+                           cudaStream_t s) {
   const unsigned g = grid_for(D.T, kWarps);
+  if (!y_split) nsplit = 0;
   if (D.dt == MOE_DT_BF16)
-    combine_kernel<__nv_bfloat16><<<g, kWarps * 32, 0, s>>>(y_perm, D.d, row_of, gate, (const __nv_bfloat16 *)x,
-                                                            D.T, D.k, D.R_max, D.flags, (__nv_bfloat16 *)y, status);
+    combine_kernel<__nv_bfloat16><<<g, kWarps * 32, 0, s>>>(y_perm, y_split, nsplit, D.d, row_of, gate,
+                                                            (const __nv_bfloat16 *)x, D.T, D.k, D.R_max, D.flags,
+                                                            (__nv_bfloat16 *)y, status);
   else
-    combine_kernel<float><<<g, kWarps * 32, 0, s>>>(y_perm, D.d, row_of, gate, (const float *)x, D.T, D.k, D.R_max,
-                                                    D.flags, (float *)y, status);
+    combine_kernel<float><<<g, kWarps * 32, 0, s>>>(y_perm, y_split, nsplit, D.d, row_of, gate, (const float *)x,
+                                                    D.T, D.k, D.R_max, D.flags, (float *)y, status);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,270 @@
+// K1 on the tensor cores: the fused router for bf16 inputs.
+//
+// "Mixture-of-Experts" (beta.fermi.ai wiki), step-by-step mechanism, steps
+// 1-3: logits x W_g, softmax over the N experts, the k largest by score,
+// renormalised to sum to 1. The projection is a [T x d] . [d x N] contraction;
+// here it runs on tcgen05 with bf16 operands and fp32 accumulation in tensor
+// memory, so every product is exact and the logits are fp32 sums, never
+// rounded to bf16 ("Inside the Router", "Mixture of Experts: How Sparse
+// Routing Scales Transformers": router logits at higher precision).
+//
+// One CTA per 128 tokens: warp 0 streams the token tile [128 x 64] and the
+// W_g tile [NP x 64] per k-block with TMA (128-byte swizzle) through a small
+// ring; warp 1 issues tcgen05.mma (M=128, N=NP, K=16) into one TMEM
+// accumulator; warps 2-5 then own one token each (TMEM lane = token): they read
+// the token's logits 32 columns at a time and do the softmax and the top-k in
+// registers (the k best kept by an unrolled insertion, ties to the lower
+// expert, picks in rank order). NP is N rounded up to 16..256; the W_g rows
+// past N are zero-filled by TMA and their columns are ignored.
+#include <math.h>
+
+#include "tc_common.cuh"
+
+namespace moe {
+namespace {
+
+using namespace tc;
+
+constexpr int kRM = 128;  // tokens per CTA (MMA M)
+constexpr int kRBK = 64;  // k-block: one 128-byte swizzle atom of bf16
+constexpr int kRThreads = 192;
+
+template <int NP> struct RCfg {
+  static constexpr int kXBytes = kRM * kRBK * 2;
+  static constexpr int kWBytes = NP * kRBK * 2;
+  static constexpr int kStageBytes = kXBytes + kWBytes;
+  static constexpr int kStages = (96 * 1024) / kStageBytes < 2 ? 2 : ((96 * 1024) / kStageBytes > 6 ? 6 : (96 * 1024) / kStageBytes);
+  static constexpr int kTmemCols = NP < 32 ? 32 : NP;  // a power of two >= 32
+};
+
+struct RCtrl {
+  unsigned long long full[8], empty[8], tfull, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int NP> constexpr size_t router_smem() {
+  return 1024 + (size_t)RCfg<NP>::kStages * RCfg<NP>::kStageBytes + sizeof(RCtrl);
+}
+
+template <int NP>
+__global__ void __launch_bounds__(kRThreads, 1)
+    router_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                     const float *__restrict__ router_bias, int64_t T_, int d, int N, int k,
+                     int32_t *__restrict__ topk_idx, float *__restrict__ gate, float *__restrict__ score,
+                     int32_t *status) {
+  using C = RCfg<NP>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t *sX = base;
+  uint8_t *sW = base + C::kStages * C::kXBytes;
+  RCtrl *c = (RCtrl *)(base + C::kStages * C::kStageBytes);
+  volatile int *abort = &c->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t t0 = (int64_t)blockIdx.x * kRM;
+  const int kb_count = (d + kRBK - 1) / kRBK;
+
+  if (warp == 1) {
+    if (lane == 0) {
+      for (int s = 0; s < C::kStages; ++s) {
+        mbar_init(&c->full[s], 1);
+        mbar_init(&c->empty[s], 1);
+      }
+      mbar_init(&c->tfull, 1);
+      mbar_init(&c->drain, 1);
+      c->abort = 0;
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&c->tmem_base)),
+                 "r"(C::kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = c->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      bool issued[8] = {false, false, false, false, false, false, false, false};
+      uint32_t issued_parity[8];
+      bool ok = true;
+      for (int kb = 0; kb < kb_count; ++kb) {
+        if (!mbar_wait_fast(&c->empty[s], ph ^ 1u, abort, status, kKRouter, 10 + s)) {
+          ok = false;
+          break;
+        }
+        mbar_expect_tx(&c->full[s], C::kStageBytes);
+        tma_load_2d(sX + s * C::kXBytes, &tm_x, &c->full[s], kb * kRBK, (int)t0);
+        tma_load_2d(sW + s * C::kWBytes, &tm_w, &c->full[s], kb * kRBK, 0);
+        issued[s] = true;
+        issued_parity[s] = ph;
+        if (++s == C::kStages) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!ok) {
+        for (int i = 0; i < C::kStages; ++i)
+          if (issued[i]) {
+            const unsigned long long ts = globaltimer();
+            while (!mbar_try_wait(&c->full[i], issued_parity[i]) && globaltimer() - ts < kTimeoutNs) {
+            }
+          }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true, any = false;
+      const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NP >> 3) << 17) |
+                             ((uint32_t)(kRM >> 4) << 24);
+      for (int kb = 0; kb < kb_count; ++kb) {
+        if (!mbar_wait_fast(&c->full[s], ph, abort, status, kKRouter, 20 + s)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t ad = smem_desc_sw128(saddr(sX + s * C::kXBytes));
+        const uint64_t bd = smem_desc_sw128(saddr(sW + s * C::kWBytes));
+#pragma unroll
+        for (int kk = 0; kk < kRBK / 16; ++kk)
+          umma_bf16_cta1(tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, (kb | kk) != 0 ? 1u : 0u);
+        any = true;
+        umma_commit_cta1(&c->empty[s]);
+        if (++s == C::kStages) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      if (ok) {
+        umma_commit_cta1(&c->tfull);
+      } else if (any) {
+        umma_commit_cta1(&c->drain);
+        const unsigned long long ts = globaltimer();
+        while (!mbar_try_wait(&c->drain, 0) && globaltimer() - ts < kTimeoutNs) {
+        }
+      }
+    }
+  } else {
+    const int q = warp & 3;
+    const int64_t t = t0 + q * 32 + lane;
+    int ok = 0;
+    if (lane == 0) ok = mbar_wait(&c->tfull, 0, abort, status, kKRouter, 30) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) {
+      tc_fence_after();
+      const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+      // pass 1: max and the k best (value desc, expert asc)
+      float m = -INFINITY;
+      float tv[8];
+      int te[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        tv[j] = -INFINITY;
+        te[j] = 0x7fffffff;
+      }
+#pragma unroll 1
+      for (int c0 = 0; c0 < NP; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(lane_base + (uint32_t)c0, r);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          int e = c0 + j;
+          if (e >= N) break;
+          float v = __uint_as_float(r[j]);
+          if (router_bias) v += router_bias[e];
+          m = fmaxf(m, v);
+#pragma unroll
+          for (int s = 0; s < 8; ++s) {
+            if (s < k && v > tv[s]) {
+              const float fv = tv[s];
+              const int fe = te[s];
+              tv[s] = v;
+              te[s] = e;
+              v = fv;
+              e = fe;
+            }
+          }
+        }
+      }
+      // pass 2: the softmax denominator
+      float sum = 0.f;
+#pragma unroll 1
+      for (int c0 = 0; c0 < NP; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(lane_base + (uint32_t)c0, r);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int e = c0 + j;
+          if (e >= N) break;
+          float v = __uint_as_float(r[j]);
+          if (router_bias) v += router_bias[e];
+          sum += expf(v - m);
+        }
+      }
+      if (t < T_) {
+        float ex[8], sel = 0.f;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          ex[s] = expf(tv[s] - m);
+          if (s < k) sel += ex[s];
+        }
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          if (s < k) {
+            topk_idx[t * k + s] = te[s];
+            score[t * k + s] = ex[s] / sum;
+            gate[t * k + s] = ex[s] / sel;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols));
+  }
+}
+
+template <int NP>
+cudaError_t launch_np(const Dims &D, const void *x, const void *w_g, const float *router_bias, int32_t *topk_idx,
+                      float *gate, float *score, int32_t *status, cudaStream_t s) {
+  static bool attr_set = false;
+  const size_t smem = router_smem<NP>();
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(router_tc_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  CUtensorMap tx, tw;
+  const uint64_t dx[2] = {(uint64_t)D.d, (uint64_t)D.T};
+  const uint64_t dw[2] = {(uint64_t)D.d, (uint64_t)D.N};
+  if (!make_map(&tx, x, 2, dx, kRM) || !make_map(&tw, w_g, 2, dw, NP)) return cudaErrorInvalidValue;
+  const unsigned grid = (unsigned)((D.T + kRM - 1) / kRM);
+  router_tc_kernel<NP><<<grid, kRThreads, smem, s>>>(tx, tw, router_bias, D.T, (int)D.d, D.N, D.k, topk_idx, gate,
+                                                     score, status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_router_tc(const Dims &D, const void *x, const void *w_g, const float *router_bias,
+                             int32_t *topk_idx, float *gate, float *score, int32_t *status, cudaStream_t s) {
+  if (D.dt != MOE_DT_BF16 || D.N > 256) return cudaErrorNotSupported;
+  if (D.N <= 16) return launch_np<16>(D, x, w_g, router_bias, topk_idx, gate, score, status, s);
+  if (D.N <= 32) return launch_np<32>(D, x, w_g, router_bias, topk_idx, gate, score, status, s);
+  if (D.N <= 64) return launch_np<64>(D, x, w_g, router_bias, topk_idx, gate, score, status, s);
+  if (D.N <= 128) return launch_np<128>(D, x, w_g, router_bias, topk_idx, gate, score, status, s);
+  return launch_np<256>(D, x, w_g, router_bias, topk_idx, gate, score, status, s);
+}
+
+}  // namespace moe

@@ -48,7 +48,7 @@ def test_capacity_stage_is_bit_exact_on_gpu_routing(w):
     assert np.array_equal(cr, g["counts_raw"])
     assert np.array_equal(ck, g["counts_kept"])
     assert np.array_equal(slot, parity.gpu_slots(g))
-    parity.check_layout(g, w.k)
+    parity.check_layout(g, w.k, parity.row_align(w))
 
 
 @pytest.mark.parametrize("w", STAGE_CASES[:3], ids=lambda w: w.name)
