@@ -41,6 +41,27 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 KERNELS_PER_STEP = 7  # router, capacity select, capacity assign, permute, GEMM1, GEMM2, combine
 
 
+def measured_traffic(workload: str):
+    """DRAM bytes per forward of the expert-FFN GEMMs from the committed ncu
+    summary (profiles/traffic.txt), or None when there is none for this
+    workload or the kernel sources changed since the capture."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        f = line.split("#", 1)[0].split()
+        if len(f) != 4 or f[0] != workload:
+            continue
+        m = hashlib.sha1()
+        for src in f[1].split(","):
+            m.update(open(os.path.join(ROOT, "sparse_mixture_experts_66_b300", "csrc", src), "rb").read())
+        if m.hexdigest()[:12] == f[2]:
+            return float(f[3])
+    return None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -292,7 +313,8 @@ def run_ours(args, world, rank, local):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "frac_of_8TBs": achieved / 8000.0,
                 "peak_source": f"{peak_src} HBM copy"}
-    roof["traffic"] = None
+    roof["traffic"] = measured_traffic(w.name)
+    roof["traffic_scope"] = "DRAM read+write bytes per forward, both GEMM launches (ncu, profiles/traffic.txt)"
     roof["kernel"] = "expert FFN: grouped GEMM1 (+b1, GELU) and GEMM2 (+b2, gate scale), 2 launches per step"
     roof["algorithmic_per_step"] = alg["flops_ffn"] if roof["bound"] == "tensor" else alg["bytes_ffn_weights"]
 
