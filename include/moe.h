@@ -108,6 +108,7 @@ typedef struct {
   size_t h;           /* dtype [rows, d_ff] expert hidden activations */
   size_t y_perm;      /* fp32  [rows, d]    gate-scaled expert outputs */
   size_t y_split;     /* fp32  [S-1, rows, d] decode-shaped configs only: the second GEMM's extra K slices */
+  size_t ffn_sync;    /* int32 [N] decode-shaped configs only: per-expert count of stored h tiles */
   size_t total;       /* bytes of the whole workspace */
   int64_t rows;       /* R_max */
   int64_t capacity;   /* C */
@@ -173,7 +174,10 @@ moe_status moe_dispatch(const moe_config *cfg, const void *x, const int32_t *top
  *   tcgen05, accumulating in tensor memory). For decode-shaped configs (bf16,
  *   T*k <= 64*N) the second GEMM is split along d_ff: y_perm receives the
  *   first slice and the workspace's y_split the others, which moe_combine
- *   (given the same workspace) adds in slice order. */
+ *   (given the same workspace) adds in slice order; both GEMMs then run in
+ *   one launch, whose second-GEMM tiles wait (bounded, MOE_ERR_TIMEOUT) on
+ *   per-expert counters in the workspace's ffn_sync, reset on the stream
+ *   before each launch. */
 moe_status moe_expert_ffn(const moe_config *cfg, const void *x_perm, const int32_t *offsets, const void *w1,
                           const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
                           float *y_perm, void *ws, moe_stream_t stream);

@@ -13,16 +13,23 @@
 // (one chunk per expert at decode sizes). Segments of the permuted buffer are
 // aligned to 64 rows in this mode, so a chunk is never pure padding.
 //
-// Persistent, one CTA per SM: warp 0 streams the weight tile [128 x 64] and
-// the token tile [64 x 64] per k-block with TMA (eight 24 KB stages); warp 1
-// issues tcgen05.mma (M=128, N=64, K=16) into one of two TMEM accumulators;
-// warps 2-5 read one accumulator lane each (TMEM lane = weight row f) and
-// store the 64 token values of that row:
+// One persistent launch, one CTA per SM, walks all GEMM1 tiles and then all
+// GEMM2 tiles (so neither GEMM leaves a partly idle last wave): warp 0 streams
+// the weight tile [128 x 64] and the token tile [64 x 64] per k-block with TMA
+// (eight 24 KB stages); warp 1 issues tcgen05.mma (M=128, N=64, K=16) into
+// one of two TMEM accumulators; warps 2-5 read one accumulator lane each
+// (TMEM lane = weight row f) and store the 64 token values of that row:
 //   GEMM1: h[off_e + j, f]      = GELU(D^T[f, j] + b1[e][f])          (bf16)
 //   GEMM2: y_s[off_e + j, o]    = g_j * (D^T[o, j] + [s == 0] b2[e][o]) (fp32)
 // GEMM2 splits K into S slices (s = 0..S-1) to give every SM work; slice s
 // writes its own partial buffer and the combine adds the S partials in a
-// fixed order, so the result stays deterministic.
+// fixed order, so the result stays deterministic. A GEMM2 tile of expert e
+// starts only when all of e's GEMM1 tiles have stored h: each epilogue warp
+// fences its generic stores for the async proxy and then increments e's
+// counter with release semantics; the producer acquires the counter (bounded
+// wait) and fences before its TMA loads of h.
+#include <vector>
+
 #include "tc_common.cuh"
 
 namespace moe {
@@ -44,35 +51,59 @@ struct DCtrl {
   unsigned long long full[kDStages], empty[kDStages], tfull[2], tempty[2], drain;
   uint32_t tmem_base;
   int abort;
-  int total_tiles;
+  int total1, total2;  // GEMM1 tiles, GEMM1 + GEMM2 tiles
   int32_t offsets[kDMaxExperts + 1];
-  int32_t tile_start[kDMaxExperts + 1];
+  int32_t start1[kDMaxExperts + 1];  // first GEMM1 tile of each expert
+  int32_t start2[kDMaxExperts + 1];  // first GEMM2 tile of each expert (counted from total1)
+};
+
+struct DTile {
+  int phase;  // 0: GEMM1, 1: GEMM2
+  int e, row0, m, sp;
 };
 
 constexpr size_t kDSmem = 1024 + (size_t)kDStages * kDStageBytes + sizeof(DCtrl);
 
-// Tiles of expert e: chunks_e x splits x m_tiles, m fastest, then the slice.
-__device__ __forceinline__ void decode_swap_tile(const DCtrl *c, int N_exp, int m_tiles, int splits, int t, int &e,
-                                                 int &row0, int &m, int &s) {
+// Tiles of expert e: chunks_e x slices x m_tiles, m fastest, then the slice.
+__device__ __forceinline__ DTile decode_tile(const DCtrl *c, int N_exp, int m1, int m2, int S, int t) {
+  DTile d;
+  d.phase = t >= c->total1 ? 1 : 0;
+  const int32_t *start = d.phase ? c->start2 : c->start1;
+  const int tt = d.phase ? t - c->total1 : t;
+  const int mt = d.phase ? m2 : m1, sl = d.phase ? S : 1;
   int lo = 0, hi = N_exp - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (c->tile_start[mid] <= t) lo = mid; else hi = mid - 1;
+    if (start[mid] <= tt) lo = mid; else hi = mid - 1;
   }
-  e = lo;
-  int local = t - c->tile_start[e];
-  m = local % m_tiles;
-  local /= m_tiles;
-  s = local % splits;
-  row0 = c->offsets[e] + (local / splits) * kDN;
+  d.e = lo;
+  int local = tt - start[lo];
+  d.m = local % mt;
+  local /= mt;
+  d.sp = local % sl;
+  d.row0 = c->offsets[lo] + (local / sl) * kDN;
+  return d;
 }
 
-template <int EPI>
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ void red_release_add(int32_t *p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire(const int32_t *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __global__ void __launch_bounds__(kDThreads, 1)
-    gemm_swap_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_t,
-                     const int32_t *__restrict__ offsets_g, int N_exp, int64_t R_max, int K, int M_out, int splits,
-                     const __nv_bfloat16 *__restrict__ bias, const float *__restrict__ row_gate,
-                     void *__restrict__ out, float *__restrict__ out_split, int64_t split_stride, int32_t *status) {
+    ffn_decode_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_x,
+                      const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_h,
+                      const int32_t *__restrict__ offsets_g, int N_exp, int64_t R_max, int d, int d_ff, int S,
+                      const __nv_bfloat16 *__restrict__ b1, const __nv_bfloat16 *__restrict__ b2,
+                      const float *__restrict__ row_gate, __nv_bfloat16 *__restrict__ h, float *__restrict__ y_perm,
+                      float *__restrict__ y_split, int32_t *__restrict__ h_done, int32_t *status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t *sW = base;
@@ -80,47 +111,58 @@ __global__ void __launch_bounds__(kDThreads, 1)
   DCtrl *c = (DCtrl *)(base + kDStages * kDStageBytes);
   volatile int *abort = &c->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m_tiles = (M_out + kDM - 1) / kDM;
-  const int kb_count = (K + kDBK - 1) / kDBK;
-  const int kb_per_split = (kb_count + splits - 1) / splits;
+  const int m1 = (d_ff + kDM - 1) / kDM, m2 = (d + kDM - 1) / kDM;
+  const int kb1_count = (d + kDBK - 1) / kDBK, kb2_count = (d_ff + kDBK - 1) / kDBK;
 
   if (warp == 0) {
-    int local[8];
-    int sum = 0;
+    int n1[8], n2[8];
+    int s1 = 0, s2 = 0;
     bool bad = false;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int e = lane * 8 + i;
-      local[i] = 0;
+      n1[i] = n2[i] = 0;
       if (e < N_exp) {
         const int o0 = offsets_g[e], o1 = offsets_g[e + 1];
         if (o1 < o0 || (o1 - o0) % kDN != 0 || o1 > R_max) bad = true;
-        else local[i] = (o1 - o0) / kDN * splits * m_tiles;
+        else {
+          n1[i] = (o1 - o0) / kDN * m1;
+          n2[i] = (o1 - o0) / kDN * S * m2;
+        }
       }
-      sum += local[i];
+      s1 += n1[i];
+      s2 += n2[i];
     }
     bad = __any_sync(0xffffffffu, bad);
-    int incl = sum;
+    int i1 = s1, i2 = s2;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += v;
+      const int v1 = __shfl_up_sync(0xffffffffu, i1, off);
+      const int v2 = __shfl_up_sync(0xffffffffu, i2, off);
+      if (lane >= off) {
+        i1 += v1;
+        i2 += v2;
+      }
     }
-    int excl = incl - sum;
+    int x1 = i1 - s1, x2 = i2 - s2;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int e = lane * 8 + i;
       if (e < N_exp) {
-        c->tile_start[e] = excl;
+        c->start1[e] = x1;
+        c->start2[e] = x2;
         c->offsets[e] = offsets_g[e];
       }
-      excl += local[i];
+      x1 += n1[i];
+      x2 += n2[i];
     }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    const int t1 = __shfl_sync(0xffffffffu, i1, 31), t2 = __shfl_sync(0xffffffffu, i2, 31);
     if (lane == 0) {
       c->offsets[N_exp] = offsets_g[N_exp];
-      c->tile_start[N_exp] = total;
-      c->total_tiles = bad ? 0 : total;
+      c->start1[N_exp] = t1;
+      c->start2[N_exp] = t2;
+      c->total1 = bad ? 0 : t1;
+      c->total2 = bad ? 0 : t1 + t2;
       c->abort = 0;
       if (bad) report_error(status, MOE_ERR_BOUNDS, kKGemmTcDecode, 1);
     }
@@ -145,32 +187,56 @@ __global__ void __launch_bounds__(kDThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const int total = c->total_tiles;
+  const int total = c->total2;
   const uint32_t tmem = c->tmem_base;
 
   if (warp == 0) {
     if (lane == 0) {
       int s = 0;
       uint32_t ph = 0;
-      bool issued[kDStages];
-      uint32_t issued_parity[kDStages];
-      for (int i = 0; i < kDStages; ++i) issued[i] = false;
+      uint32_t issued_mask = 0, parity_mask = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-        int e, row0, m, sp;
-        decode_swap_tile(c, N_exp, m_tiles, splits, t, e, row0, m, sp);
-        const int kb0 = sp * kb_per_split;
-        const int kb1 = min(kb_count, kb0 + kb_per_split);
+        const DTile tl = decode_tile(c, N_exp, m1, m2, S, t);
+        int kb0 = 0, kb1 = kb1_count;
+        if (tl.phase) {
+          kb0 = tl.sp * kb2_count / S;
+          kb1 = (tl.sp + 1) * kb2_count / S;
+          // every GEMM1 tile of this expert must have stored its rows of h
+          const int need = (c->offsets[tl.e + 1] - c->offsets[tl.e]) / kDN * m1 * 4;
+          if (ld_acquire(h_done + tl.e) < need) {
+            const unsigned long long ts = globaltimer();
+            while (ld_acquire(h_done + tl.e) < need) {
+              if (*abort) {
+                ok = false;
+                break;
+              }
+              if (globaltimer() - ts > kTimeoutNs) {
+                report_error(status, MOE_ERR_TIMEOUT, kKGemmTcDecode, 5);
+                *abort = 1;
+                ok = false;
+                break;
+              }
+            }
+            if (!ok) break;
+          }
+          fence_proxy_async_global();
+        }
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_fast(&c->empty[s], ph ^ 1u, abort, status, kKGemmTcDecode, 10 + s)) {
             ok = false;
             break;
           }
           mbar_expect_tx(&c->full[s], kDStageBytes);
-          tma_load_3d(sW + s * kDWBytes, &tm_w, &c->full[s], kb * kDBK, m * kDM, e);
-          tma_load_2d(sT + s * kDTBytes, &tm_t, &c->full[s], kb * kDBK, row0);
-          issued[s] = true;
-          issued_parity[s] = ph;
+          if (tl.phase == 0) {
+            tma_load_3d(sW + s * kDWBytes, &tm_w1, &c->full[s], kb * kDBK, tl.m * kDM, tl.e);
+            tma_load_2d(sT + s * kDTBytes, &tm_x, &c->full[s], kb * kDBK, tl.row0);
+          } else {
+            tma_load_3d(sW + s * kDWBytes, &tm_w2, &c->full[s], kb * kDBK, tl.m * kDM, tl.e);
+            tma_load_2d(sT + s * kDTBytes, &tm_h, &c->full[s], kb * kDBK, tl.row0);
+          }
+          issued_mask |= 1u << s;
+          parity_mask = (parity_mask & ~(1u << s)) | (ph << s);
           if (++s == kDStages) {
             s = 0;
             ph ^= 1u;
@@ -179,9 +245,9 @@ __global__ void __launch_bounds__(kDThreads, 1)
       }
       if (!ok) {
         for (int i = 0; i < kDStages; ++i)
-          if (issued[i]) {
+          if (issued_mask & (1u << i)) {
             const unsigned long long ts = globaltimer();
-            while (!mbar_try_wait(&c->full[i], issued_parity[i]) && globaltimer() - ts < kTimeoutNs) {
+            while (!mbar_try_wait(&c->full[i], (parity_mask >> i) & 1u) && globaltimer() - ts < kTimeoutNs) {
             }
           }
       }
@@ -194,16 +260,14 @@ __global__ void __launch_bounds__(kDThreads, 1)
       bool ok = true, any = false;
       const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kDN >> 3) << 17) |
                              ((uint32_t)(kDM >> 4) << 24);
-      uint64_t wdesc[kDStages], tdesc[kDStages];
-      for (int i = 0; i < kDStages; ++i) {
-        wdesc[i] = smem_desc_sw128(saddr(sW + i * kDWBytes));
-        tdesc[i] = smem_desc_sw128(saddr(sT + i * kDTBytes));
-      }
+      const uint64_t wdesc0 = smem_desc_sw128(saddr(sW)), tdesc0 = smem_desc_sw128(saddr(sT));
       for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-        int e, row0, m, sp;
-        decode_swap_tile(c, N_exp, m_tiles, splits, t, e, row0, m, sp);
-        const int kb0 = sp * kb_per_split;
-        const int kb1 = min(kb_count, kb0 + kb_per_split);
+        const DTile tl = decode_tile(c, N_exp, m1, m2, S, t);
+        int kb0 = 0, kb1 = kb1_count;
+        if (tl.phase) {
+          kb0 = tl.sp * kb2_count / S;
+          kb1 = (tl.sp + 1) * kb2_count / S;
+        }
         if (!mbar_wait_fast(&c->tempty[acc], aph ^ 1u, abort, status, kKGemmTcDecode, 20 + acc)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + (uint32_t)(acc * kDN);
@@ -215,7 +279,8 @@ __global__ void __launch_bounds__(kDThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kDBK / 16; ++kk)
-            umma_bf16_cta1(d_tmem, wdesc[s] + (uint64_t)(2 * kk), tdesc[s] + (uint64_t)(2 * kk), idesc,
+            umma_bf16_cta1(d_tmem, wdesc0 + (uint64_t)(s * (kDWBytes >> 4) + 2 * kk),
+                           tdesc0 + (uint64_t)(s * (kDTBytes >> 4) + 2 * kk), idesc,
                            (kb != kb0 || kk != 0) ? 1u : 0u);
           any = true;
           umma_commit_cta1(&c->empty[s]);
@@ -241,36 +306,45 @@ __global__ void __launch_bounds__(kDThreads, 1)
     int acc = 0;
     uint32_t aph = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      int e, row0, m, sp;
-      decode_swap_tile(c, N_exp, m_tiles, splits, t, e, row0, m, sp);
+      const DTile tl = decode_tile(c, N_exp, m1, m2, S, t);
       int ok = 0;
       if (lane == 0) ok = mbar_wait(&c->tfull[acc], aph, abort, status, kKGemmTcDecode, 40 + acc) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const int f = m * kDM + q * 32 + lane;  // this thread's weight row (output feature)
+      const int M_out = tl.phase ? d : d_ff;
+      const int f = tl.m * kDM + q * 32 + lane;  // this thread's weight row (output feature)
       const bool fvalid = f < M_out;
       float b = 0.f;
-      if (fvalid && (EPI == 1 || sp == 0)) b = __bfloat162float(bias[(int64_t)e * M_out + f]);
+      if (fvalid && (tl.phase == 0 || tl.sp == 0))
+        b = __bfloat162float((tl.phase ? b2 : b1)[(int64_t)tl.e * M_out + f]);
+      float *dst = tl.phase ? (tl.sp == 0 ? y_perm : y_split + (int64_t)(tl.sp - 1) * R_max * d) : nullptr;
 #pragma unroll 1
       for (int c0 = 0; c0 < kDN; c0 += 32) {
         uint32_t r[32];
         __syncwarp();
         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kDN + c0), r);
         if (fvalid) {
+          if (tl.phase == 0) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int64_t row = (int64_t)row0 + c0 + j;
-            const float v = __uint_as_float(r[j]) + b;
-            if (EPI == 1) {
-              ((__nv_bfloat16 *)out)[row * M_out + f] = __float2bfloat16_rn(gelu_as(v));
-            } else {
+            for (int j = 0; j < 32; ++j) {
+              const int64_t row = (int64_t)tl.row0 + c0 + j;
+              h[row * d_ff + f] = __float2bfloat16_rn(gelu_as(__uint_as_float(r[j]) + b));
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int64_t row = (int64_t)tl.row0 + c0 + j;
               const float g = row_gate ? row_gate[row] : 1.0f;
-              float *dst = sp == 0 ? (float *)out : out_split + (int64_t)(sp - 1) * split_stride;
-              dst[row * M_out + f] = g * v;
+              dst[row * d + f] = g * (__uint_as_float(r[j]) + b);
             }
           }
         }
+      }
+      if (tl.phase == 0) {
+        fence_proxy_async_global();  // h stores before the async-proxy loads of GEMM2 tiles
+        __syncwarp();
+        if (lane == 0) red_release_add(h_done + tl.e, 1);
       }
       tc_fence_before();
       __syncwarp();
@@ -288,54 +362,109 @@ __global__ void __launch_bounds__(kDThreads, 1)
   }
 }
 
-template <int EPI>
-cudaError_t launch_swap(const Dims &D, const void *W, const void *A, int64_t K, int64_t M_out, int splits,
-                        const void *bias, const float *row_gate, const int32_t *offsets, void *out,
-                        float *out_split, int32_t *status, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_swap_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kDSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  CUtensorMap tw, tt;
-  const uint64_t dw[3] = {(uint64_t)K, (uint64_t)M_out, (uint64_t)D.N};
-  const uint64_t dt[2] = {(uint64_t)K, (uint64_t)D.R_max};
-  if (!make_map(&tw, W, 3, dw, kDM) || !make_map(&tt, A, 2, dt, kDN)) return cudaErrorInvalidValue;
-  const int64_t max_tiles = (D.R_max / kDN) * splits * ((M_out + kDM - 1) / kDM);
-  int grid = num_sms();
-  if (max_tiles < grid) grid = (int)max_tiles;
-  if (grid < 1) grid = 1;
-  gemm_swap_kernel<EPI><<<grid, kDThreads, kDSmem, s>>>(tw, tt, offsets, D.N, D.R_max, (int)K, (int)M_out, splits,
-                                                         (const __nv_bfloat16 *)bias, row_gate, out, out_split,
-                                                         D.R_max * M_out, status);
-  return cudaGetLastError();
-}
-
 }  // namespace
+
+// Largest number of k-blocks one CTA streams when the tiles are dealt out
+// round-robin (tile t to CTA t mod sms) in the kernel's order: all GEMM1
+// tiles, then per chunk the S slices of m2 tiles each.
+static int64_t max_cta_kblocks(int64_t chunks, int64_t m1, int64_t kb1, int64_t m2, int64_t kb2, int64_t S,
+                               int64_t sms) {
+  std::vector<int64_t> diff((size_t)sms + 1, 0);
+  int64_t all = 0, p = 0;
+  auto segment = [&](int64_t n, int64_t w) {
+    all += n / sms * w;
+    const int64_t rem = n % sms, a = (p + n - rem) % sms;
+    if (rem > 0) {
+      if (a + rem <= sms) {
+        diff[(size_t)a] += w;
+        diff[(size_t)(a + rem)] -= w;
+      } else {
+        diff[(size_t)a] += w;
+        diff[(size_t)sms] -= w;
+        diff[0] += w;
+        diff[(size_t)(a + rem - sms)] -= w;
+      }
+    }
+    p += n;
+  };
+  segment(chunks * m1, kb1);
+  for (int64_t c = 0; c < chunks; ++c)
+    for (int64_t sp = 0; sp < S; ++sp) segment(m2, (sp + 1) * kb2 / S - sp * kb2 / S);
+  int64_t run = 0, mx = 0;
+  for (int64_t i = 0; i < sms; ++i) {
+    run += diff[(size_t)i];
+    mx = run > mx ? run : mx;
+  }
+  return all + mx;
+}
 
 int decode_splits(const Dims &D) {
   if (D.dt != MOE_DT_BF16 || D.T * (int64_t)D.k > (int64_t)kDecodeRowsPerExpert * D.N) return 0;
-  // K slices of the second GEMM so that the tiles cover every SM about four times
-  const int64_t tiles = (int64_t)D.N * ((D.d + kDM - 1) / kDM);
-  int64_t s = (4 * 148 + tiles - 1) / tiles;
-  const int64_t kb = (D.d_ff + kDBK - 1) / kDBK;
-  if (s > kb / 4) s = kb / 4;
-  if (s > 8) s = 8;
-  if (s < 1) s = 1;
-  return (int)s;
+  // K slices of the second GEMM. The busiest CTA's weight stream sets the
+  // time; every slice past the first adds a [rows, d] fp32 partial written
+  // here and read by the combine. Pick the S (1..8, at least 4 k-blocks per
+  // slice) that minimises the sum, for one 64-row chunk per routed expert.
+  const int64_t m1 = (D.d_ff + kDM - 1) / kDM, m2 = (D.d + kDM - 1) / kDM;
+  const int64_t kb1 = (D.d + kDBK - 1) / kDBK, kb2 = (D.d_ff + kDBK - 1) / kDBK;
+  const int64_t sms = num_sms();
+  const int64_t tk = D.T * (int64_t)D.k;
+  const int64_t chunks = tk < D.N ? (tk > 0 ? tk : 1) : D.N;
+  const double tile_bytes = (double)kDM * kDBK * 2;
+  int best = 1;
+  double best_cost = 0.0;
+  for (int64_t S = 1; S <= 8 && (S == 1 || S <= kb2 / 4); ++S) {
+    const double cost = (double)max_cta_kblocks(chunks, m1, kb1, m2, kb2, S, sms) * tile_bytes * (double)sms +
+                        (double)(S - 1) * 2.0 * (double)chunks * kDN * (double)D.d * 4.0;
+    if (S == 1 || cost < best_cost) {
+      best_cost = cost;
+      best = (int)S;
+    }
+  }
+  return best;
 }
 
 cudaError_t launch_ffn_decode(const Dims &D, const void *x_perm, const int32_t *offsets, const void *w1,
                               const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
-                              float *y_perm, float *y_split, int32_t *status, cudaStream_t s) {
+                              float *y_perm, float *y_split, int32_t *h_done, int32_t *status, cudaStream_t s) {
   const int S = decode_splits(D);
-  if (S < 1 || (S > 1 && !y_split)) return cudaErrorNotSupported;
-  cudaError_t e = launch_swap<1>(D, w1, x_perm, D.d, D.d_ff, 1, b1, nullptr, offsets, h, nullptr, status, s);
+  if (S < 1 || (S > 1 && !y_split) || !h_done || D.N > kDMaxExperts) return cudaErrorNotSupported;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(ffn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  CUtensorMap tw1, tx, tw2, th;
+  const uint64_t dw1[3] = {(uint64_t)D.d, (uint64_t)D.d_ff, (uint64_t)D.N};
+  const uint64_t dx[2] = {(uint64_t)D.d, (uint64_t)D.R_max};
+  const uint64_t dw2[3] = {(uint64_t)D.d_ff, (uint64_t)D.d, (uint64_t)D.N};
+  const uint64_t dh[2] = {(uint64_t)D.d_ff, (uint64_t)D.R_max};
+  if (!make_map(&tw1, w1, 3, dw1, kDM) || !make_map(&tx, x_perm, 2, dx, kDN) || !make_map(&tw2, w2, 3, dw2, kDM) ||
+      !make_map(&th, h, 2, dh, kDN))
+    return cudaErrorInvalidValue;
+  // h_done counts, per expert, the epilogue warps that finished a GEMM1 tile
+  cudaError_t e = cudaMemsetAsync(h_done, 0, sizeof(int32_t) * D.N, s);
   if (e != cudaSuccess) return e;
-  // K slice 0 writes y_perm; slice s >= 1 writes y_split + (s - 1) * R_max * d
-  return launch_swap<2>(D, w2, h, D.d_ff, D.d, S, b2, row_gate, offsets, y_perm, y_split, status, s);
+  const int64_t chunks = D.R_max / kDN;
+  const int64_t max_tiles = chunks * ((D.d_ff + kDM - 1) / kDM) + chunks * S * ((D.d + kDM - 1) / kDM);
+  int grid = num_sms();
+  if (max_tiles < grid) grid = (int)max_tiles;
+  if (grid < 1) grid = 1;
+  // A cooperative launch: every CTA is resident at once, so a second-GEMM tile
+  // never waits on a first-GEMM tile of a CTA that has not started.
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)grid);
+  lc.blockDim = dim3(kDThreads);
+  lc.dynamicSmemBytes = kDSmem;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, ffn_decode_kernel, tw1, tx, tw2, th, offsets, (int)D.N, (int64_t)D.R_max, (int)D.d,
+                            (int)D.d_ff, S, (const __nv_bfloat16 *)b1, (const __nv_bfloat16 *)b2, row_gate,
+                            (__nv_bfloat16 *)h, y_perm, y_split, h_done, status);
 }
 
 }  // namespace moe

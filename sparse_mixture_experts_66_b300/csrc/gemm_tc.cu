@@ -233,12 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int s = 0;
       uint32_t ph = 0;
-      bool issued[kStagesP];
-      uint32_t issued_parity[kStagesP];
-      for (int i = 0; i < kStagesP; ++i) issued[i] = false;
+      uint32_t issued_mask = 0, parity_mask = 0;  // stages with a copy issued, and its phase parity
       bool ok = true;
-      uint32_t full_leader[kStagesP];
-      for (int i = 0; i < kStagesP; ++i) full_leader[i] = map_to_rank(saddr(&c->full[i]), 0);
+      // the leader's full barriers: consecutive 8-byte objects, mapped once
+      const uint32_t full_leader0 = map_to_rank(saddr(&c->full[0]), 0);
       for (int t = pair; ok && t < total; t += npairs) {
         int e, m0, ni;
         decode_pair_tile(c, N_exp, t, e, m0, ni);
@@ -249,10 +247,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           if (rank == 0) mbar_expect_tx(&c->full[s], 2 * kStageP);
-          tma_load_2d_pair(sA + s * kAP, &tm_a, full_leader[s], kb * BK, a_row);
-          tma_load_3d_pair(sB + s * kBP, &tm_b, full_leader[s], kb * BK, b_row, e);
-          issued[s] = true;
-          issued_parity[s] = ph;
+          const uint32_t full_leader = full_leader0 + 8u * (uint32_t)s;
+          tma_load_2d_pair(sA + s * kAP, &tm_a, full_leader, kb * BK, a_row);
+          tma_load_3d_pair(sB + s * kBP, &tm_b, full_leader, kb * BK, b_row, e);
+          issued_mask |= 1u << s;
+          parity_mask = (parity_mask & ~(1u << s)) | (ph << s);
           if (++s == kStagesP) {
             s = 0;
             ph ^= 1u;
@@ -261,9 +260,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok && rank == 0) {  // the leader's full barriers track both CTAs' copies: drain them
         for (int i = 0; i < kStagesP; ++i)
-          if (issued[i]) {
+          if (issued_mask & (1u << i)) {
             const unsigned long long t0 = globaltimer();
-            while (!mbar_try_wait(&c->full[i], issued_parity[i]) && globaltimer() - t0 < kTimeoutNs) {
+            while (!mbar_try_wait(&c->full[i], (parity_mask >> i) & 1u) && globaltimer() - t0 < kTimeoutNs) {
             }
           }
       }
@@ -276,11 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true, any = false;
       const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BNP >> 3) << 17) |
                              ((uint32_t)((2 * BM) >> 4) << 24);
-      uint64_t adesc[kStagesP], bdesc[kStagesP];
-      for (int i = 0; i < kStagesP; ++i) {
-        adesc[i] = smem_desc_sw128(saddr(sA + i * kAP));
-        bdesc[i] = smem_desc_sw128(saddr(sB + i * kBP));
-      }
+      // stage buffers are equally spaced: a stage's descriptor is the first one
+      // advanced by the stage offset in 16-byte units (no carry out of the
+      // 14-bit address field below 256 KB)
+      const uint64_t adesc0 = smem_desc_sw128(saddr(sA)), bdesc0 = smem_desc_sw128(saddr(sB));
       for (int t = pair; ok && t < total; t += npairs) {
         if (!mbar_wait_fast(&c->tempty[acc], aph ^ 1u, abort, status, kKGemmTc, 60 + acc)) break;
         tc_fence_after();
@@ -291,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t ad = adesc[s], bd = bdesc[s];
+          const uint64_t ad = adesc0 + (uint64_t)(s * (kAP >> 4)), bd = bdesc0 + (uint64_t)(s * (kBP >> 4));
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             umma_bf16_pair(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, (kb | kk) != 0 ? 1u : 0u);

@@ -94,6 +94,7 @@ void make_layout(const Dims &D, moe_workspace_layout *L) {
   L->y_perm = take(R * (size_t)D.d * 4);
   const int S = decode_splits(D);
   L->y_split = take(S > 1 ? (size_t)(S - 1) * R * (size_t)D.d * 4 : 0);
+  L->ffn_sync = take(S > 0 ? N * 4 : 0);
   L->total = off;
   L->rows = D.R_max;
   L->capacity = D.C;
@@ -150,7 +151,7 @@ moe_status do_ffn(const Dims &D, const moe_workspace_layout &L, const void *x_pe
   int32_t *status = AT(ws, L.status, int32_t *);
   if (decode_splits(D) > 0) {
     cudaError_t e = launch_ffn_decode(D, x_perm, offsets, w1, b1, w2, b2, row_gate, h, y_perm,
-                                      AT(ws, L.y_split, float *), status, s);
+                                      AT(ws, L.y_split, float *), AT(ws, L.ffn_sync, int32_t *), status, s);
     if (e == cudaErrorNotSupported)
       return fail(MOE_ERR_UNSUPPORTED, "expert FFN: decode shape not supported by the tensor-core kernels");
     if (e != cudaSuccess) return cuda_fail(e, "expert FFN (decode, tensor cores)");

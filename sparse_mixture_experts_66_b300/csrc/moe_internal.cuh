@@ -107,11 +107,12 @@ int decode_splits(const Dims &D);
 // Segment alignment of the permuted buffers for this config.
 inline int row_align(const Dims &D) { return decode_splits(D) > 0 ? kDecodeRowsPerExpert : kRowAlign; }
 
-// Swap-AB expert FFNs for decode-shaped batches. y_split holds the second
-// GEMM's K slices 1..S-1 (S = decode_splits), each [R_max, d] fp32.
+// Swap-AB expert FFNs for decode-shaped batches, both GEMMs in one launch.
+// y_split holds the second GEMM's K slices 1..S-1 (S = decode_splits), each
+// [R_max, d] fp32; h_done [N] int32 is reset here and counts stored h tiles.
 cudaError_t launch_ffn_decode(const Dims &D, const void *x_perm, const int32_t *offsets, const void *w1,
                               const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
-                              float *y_perm, float *y_split, int32_t *status, cudaStream_t s);
+                              float *y_perm, float *y_split, int32_t *h_done, int32_t *status, cudaStream_t s);
 
 cudaError_t launch_permute(const Dims &D, const void *x, const int32_t *offsets, const int32_t *row_token,
                            void *x_perm, int32_t *status, cudaStream_t s);

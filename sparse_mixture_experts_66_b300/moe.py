@@ -58,7 +58,7 @@ class MoeConfig(ctypes.Structure):
 class MoeWorkspaceLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "status", "topk_idx", "gate", "score", "counts_raw", "counts_kept", "offsets", "sel_thr", "sel_eq",
-        "row_of", "row_token", "row_gate", "x_perm", "h", "y_perm", "y_split", "total")] + [
+        "row_of", "row_token", "row_gate", "x_perm", "h", "y_perm", "y_split", "ffn_sync", "total")] + [
         ("rows", ctypes.c_int64), ("capacity", ctypes.c_int64)]
 
 

@@ -72,7 +72,7 @@ def test_workspace_layout_is_aligned_and_sized():
         L = moe.moe_get_workspace_layout(cfg)
         S = min(w.T * w.k, w.N * L.capacity)
         assert L.rows == (S + 127 * w.N) // 128 * 128
-        offs = [getattr(L, f) for f, _ in moe.MoeWorkspaceLayout._fields_[:16]]
+        offs = [getattr(L, f) for f, _ in moe.MoeWorkspaceLayout._fields_[:17]]
         assert all(o % 256 == 0 for o in offs)
         assert offs == sorted(offs)
         es = 2 if w.dtype == "bf16" else 4
