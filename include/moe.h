@@ -183,7 +183,9 @@ moe_status moe_expert_ffn(const moe_config *cfg, const void *x_perm, const int32
                           float *y_perm, void *ws, moe_stream_t stream);
 
 /* Step 7: y[t] = sum over j < k with row_of[t,j] >= 0, in j order, of
- * y_perm[row_of[t,j]], in fp32, stored in dtype. No atomics.
+ * y_perm[row_of[t,j]], in fp32, stored in dtype. No atomics. For
+ * decode-shaped configs each pick's term is first completed with the same row
+ * of the workspace's y_split slices, added in slice order.
  *   gate [T, k] is read only under MOE_FLAG_RENORM_SURVIVORS (the sum is then
  *   divided by the token's kept-gate sum); x [T, d] only under
  *   MOE_FLAG_IDENTITY_FALLBACK (a token with no kept pick outputs x_t). Either

@@ -124,7 +124,7 @@ moe_status check_opt(const void *p, const char *what) {
 moe_status do_route(const Dims &D, const moe_workspace_layout &L, const void *x, const void *w_g,
                     const float *router_bias, int32_t *topk_idx, float *gate, float *score, void *ws,
                     cudaStream_t s) {
-  cudaError_t e = D.dt == MOE_DT_BF16
+  cudaError_t e = D.dt == MOE_DT_BF16 && !router_split(D)
                       ? launch_router_tc(D, x, w_g, router_bias, topk_idx, gate, score, AT(ws, L.status, int32_t *), s)
                       : launch_router(D, x, w_g, router_bias, topk_idx, gate, score, AT(ws, L.status, int32_t *), s);
   if (e != cudaSuccess) return cuda_fail(e, "router launch");

@@ -89,6 +89,11 @@ __device__ __forceinline__ int segment_of(const int32_t *offsets, int N, int64_t
 void set_last_error(const char *text);
 
 // ---- launchers (each returns the launch's cudaError_t) ----
+// Batches small enough that the router splits each token's columns over a
+// CTA's warps (few tokens would leave most SMs idle otherwise).
+constexpr int64_t kSplitRouterMaxT = 1024;
+inline bool router_split(const Dims &D) { return D.T <= kSplitRouterMaxT; }
+
 cudaError_t launch_router(const Dims &D, const void *x, const void *w_g, const float *router_bias,
                           int32_t *topk_idx, float *gate, float *score, int32_t *status, cudaStream_t s);
 

@@ -18,6 +18,7 @@ namespace moe {
 namespace {
 
 constexpr int kWarps = 8;
+constexpr int kCombineThreads = 256;
 
 __global__ void __launch_bounds__(kWarps * 32) permute_kernel(const uint4 *__restrict__ x, int64_t vec_per_row,
                                                               const int32_t *__restrict__ offsets, int N,
@@ -69,81 +70,146 @@ template <> struct Store4<__nv_bfloat16> {
   }
 };
 
-template <typename T>
-__global__ void __launch_bounds__(kWarps * 32) combine_kernel(const float *__restrict__ y_perm,
-                                                              const float *__restrict__ y_split, int nsplit,
-                                                              int64_t d,
-                                                              const int32_t *__restrict__ row_of,
-                                                              const float *__restrict__ gate,
-                                                              const T *__restrict__ x, int64_t T_, int k,
-                                                              int64_t R_max, uint32_t flags, T *__restrict__ y,
-                                                              int32_t *status) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int64_t t = (int64_t)blockIdx.x * kWarps + warp; t < T_; t += (int64_t)gridDim.x * kWarps) {
-    int32_t rows[8];
-    int nkept = 0;
-    float kept_gate = 0.f;
+// Combine, without K slices: each thread owns 4 columns of U tokens
+// (U = 8 / KM, KM >= k), so a thread first has U x KM row indices and then
+// U x KM 16-byte rows in flight at once; the loads are unconditional (a
+// dropped pick reads row 0 and is masked out), so nothing serialises them.
+// The picks of a token are added in pick order.
+template <typename T, int KM>
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float *__restrict__ y_perm, int64_t d,
+                                                                  const int32_t *__restrict__ row_of,
+                                                                  const float *__restrict__ gate,
+                                                                  const T *__restrict__ x, int64_t T_, int k,
+                                                                  int64_t R_max, uint32_t flags,
+                                                                  T *__restrict__ y, int32_t *status) {
+  constexpr int U = 8 / KM;
+  const int64_t d4 = d >> 2;
+  const int64_t items = T_ * d4;
+  int64_t tok[U], col[U];
+  int32_t rows[U][KM];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      rows[j] = -1;
-      if (j < k) {
-        int32_t r = row_of[t * k + j];
-        if (r >= R_max) {
-          if (lane == 0) report_error(status, MOE_ERR_BOUNDS, kKCombine, (int32_t)t);
-          r = -1;
-        }
-        rows[j] = r;
-        if (r >= 0) {
-          ++nkept;
-          if (flags & MOE_FLAG_RENORM_SURVIVORS) kept_gate += gate[t * k + j];
-        }
-      }
+  for (int u = 0; u < U; ++u) {
+    const int64_t i = ((int64_t)blockIdx.x * U + u) * kCombineThreads + threadIdx.x;
+    tok[u] = i < items ? i / d4 : -1;
+    col[u] = i < items ? (i - tok[u] * d4) << 2 : 0;
+#pragma unroll
+    for (int j = 0; j < KM; ++j) rows[u][j] = (tok[u] >= 0 && j < k) ? __ldg(row_of + tok[u] * k + j) : -1;
+  }
+  float4 acc[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    float4 v[KM];
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+      const int64_t r = (rows[u][j] >= 0 && rows[u][j] < R_max) ? rows[u][j] : 0;
+      v[j] = __ldg(reinterpret_cast<const float4 *>(y_perm + r * d + col[u]));
     }
-    const bool renorm = (flags & MOE_FLAG_RENORM_SURVIVORS) && nkept > 0;
-    const bool identity = (flags & MOE_FLAG_IDENTITY_FALLBACK) && nkept == 0;
-    constexpr int B = 4;  // column groups per pass: B loads per kept pick in flight
-    for (int64_t c0 = (int64_t)lane * 4; c0 < d; c0 += 128 * B) {
-      float4 acc[B];
+    acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int b = 0; b < B; ++b) acc[b] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (rows[j] >= 0) {
-          // the pick's row: y_perm, then the K slices of a decode-mode GEMM in order
-          for (int sl = 0; sl <= nsplit; ++sl) {
-            float4 v[B];
-            const float *src = (sl == 0 ? y_perm : y_split + (int64_t)(sl - 1) * R_max * d) + (int64_t)rows[j] * d;
-#pragma unroll
-            for (int b = 0; b < B; ++b)
-              if (c0 + 128 * b < d) v[b] = __ldg(reinterpret_cast<const float4 *>(src + c0 + 128 * b));
-#pragma unroll
-            for (int b = 0; b < B; ++b) {
-              if (c0 + 128 * b < d) {
-                acc[b].x += v[b].x;
-                acc[b].y += v[b].y;
-                acc[b].z += v[b].z;
-                acc[b].w += v[b].w;
-              }
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int b = 0; b < B; ++b) {
-        const int64_t c = c0 + 128 * b;
-        if (c >= d) continue;
-        float4 a = acc[b];
-        if (renorm) {
-          a.x /= kept_gate;
-          a.y /= kept_gate;
-          a.z /= kept_gate;
-          a.w /= kept_gate;
-        }
-        if (identity) a = Store4<T>::ld(x + t * d + c);
-        Store4<T>::st(y + t * d + c, a);
+    for (int j = 0; j < KM; ++j) {
+      if (rows[u][j] >= 0 && rows[u][j] < R_max) {
+        acc[u].x += v[j].x;
+        acc[u].y += v[j].y;
+        acc[u].z += v[j].z;
+        acc[u].w += v[j].w;
       }
     }
   }
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    if (tok[u] < 0) continue;
+    int nkept = 0;
+    float kept_gate = 0.f;
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+      if (rows[u][j] >= R_max && col[u] == 0) report_error(status, MOE_ERR_BOUNDS, kKCombine, (int32_t)tok[u]);
+      if (rows[u][j] >= 0 && rows[u][j] < R_max) {
+        ++nkept;
+        if (flags & MOE_FLAG_RENORM_SURVIVORS) kept_gate += __ldg(gate + tok[u] * k + j);
+      }
+    }
+    float4 a = acc[u];
+    if ((flags & MOE_FLAG_RENORM_SURVIVORS) && nkept > 0) {
+      a.x /= kept_gate;
+      a.y /= kept_gate;
+      a.z /= kept_gate;
+      a.w /= kept_gate;
+    }
+    if ((flags & MOE_FLAG_IDENTITY_FALLBACK) && nkept == 0) a = Store4<T>::ld(x + tok[u] * d + col[u]);
+    Store4<T>::st(y + tok[u] * d + col[u], a);
+  }
+}
+
+// Combine with the K slices of a decode-mode second GEMM: one thread per
+// (token, 4 columns); the k x (1 + nsplit) source rows are walked as one flat
+// list, 8 loads at a time. Per pick the slices are added in slice order, then
+// the picks in pick order.
+template <typename T>
+__global__ void __launch_bounds__(kCombineThreads) combine_split_kernel(
+    const float *__restrict__ y_perm, const float *__restrict__ y_split, int nsplit, int64_t d,
+    const int32_t *__restrict__ row_of, const float *__restrict__ gate, const T *__restrict__ x, int64_t T_, int k,
+    int64_t R_max, uint32_t flags, T *__restrict__ y, int32_t *status) {
+  const int64_t d4 = d >> 2;
+  const int64_t i = (int64_t)blockIdx.x * kCombineThreads + threadIdx.x;
+  if (i >= T_ * d4) return;
+  const int64_t t = i / d4;
+  const int64_t c = (i - t * d4) << 2;
+  const int per = 1 + nsplit, nsrc = k * per;
+  uint32_t kept = 0;  // bit j: pick j kept
+  float kept_gate = 0.f;
+  for (int j = 0; j < k; ++j) {
+    const int32_t r = __ldg(row_of + t * k + j);
+    if (r >= R_max && c == 0) report_error(status, MOE_ERR_BOUNDS, kKCombine, (int32_t)t);
+    if (r >= 0 && r < R_max) {
+      kept |= 1u << j;
+      if (flags & MOE_FLAG_RENORM_SURVIVORS) kept_gate += __ldg(gate + t * k + j);
+    }
+  }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), part = acc;
+  for (int q0 = 0; q0 < nsrc; q0 += 8) {
+    float4 v[8];
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const int q = q0 + b;
+      const int j = q / per, sl = q - j * per;
+      const float *src = y_perm;
+      int64_t r = 0;
+      if (q < nsrc) {
+        const int32_t rr = __ldg(row_of + t * k + j);
+        r = (rr >= 0 && rr < R_max) ? rr : 0;
+        if (sl > 0) src = y_split + (int64_t)(sl - 1) * R_max * d;
+      }
+      v[b] = __ldg(reinterpret_cast<const float4 *>(src + r * d + c));
+    }
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const int q = q0 + b;
+      if (q < nsrc) {
+        const int j = q / per, sl = q - j * per;
+        part.x += v[b].x;
+        part.y += v[b].y;
+        part.z += v[b].z;
+        part.w += v[b].w;
+        if (sl == nsplit) {
+          if (kept & (1u << j)) {
+            acc.x += part.x;
+            acc.y += part.y;
+            acc.z += part.z;
+            acc.w += part.w;
+          }
+          part = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+    }
+  }
+  if ((flags & MOE_FLAG_RENORM_SURVIVORS) && kept) {
+    acc.x /= kept_gate;
+    acc.y /= kept_gate;
+    acc.z /= kept_gate;
+    acc.w /= kept_gate;
+  }
+  if ((flags & MOE_FLAG_IDENTITY_FALLBACK) && !kept) acc = Store4<T>::ld(x + t * d + c);
+  Store4<T>::st(y + t * d + c, acc);
 }
 
 unsigned grid_for(int64_t items, int per_block) {
@@ -165,19 +231,47 @@ cudaError_t launch_permute(const Dims &D, const void *x, const int32_t *offsets,
   return cudaGetLastError();
 }
 
+namespace {
+template <typename T>
+cudaError_t launch_combine_t(const Dims &D, const float *y_perm, const float *y_split, int nsplit,
+                             const int32_t *row_of, const float *gate, const T *x, T *y, int32_t *status,
+                             cudaStream_t s) {
+  const int64_t items = D.T * (D.d / 4);
+  if (nsplit > 0) {
+    const int64_t g = (items + kCombineThreads - 1) / kCombineThreads;
+    combine_split_kernel<T><<<(unsigned)g, kCombineThreads, 0, s>>>(y_perm, y_split, nsplit, D.d, row_of, gate, x,
+                                                                    D.T, D.k, D.R_max, D.flags, y, status);
+    return cudaGetLastError();
+  }
+  const int km = D.k <= 1 ? 1 : D.k <= 2 ? 2 : D.k <= 4 ? 4 : 8;
+  const int64_t per_block = (int64_t)kCombineThreads * (8 / km);
+  const unsigned g = (unsigned)((items + per_block - 1) / per_block);
+  if (km == 1)
+    combine_kernel<T, 1><<<g, kCombineThreads, 0, s>>>(y_perm, D.d, row_of, gate, x, D.T, D.k, D.R_max, D.flags, y,
+                                                       status);
+  else if (km == 2)
+    combine_kernel<T, 2><<<g, kCombineThreads, 0, s>>>(y_perm, D.d, row_of, gate, x, D.T, D.k, D.R_max, D.flags, y,
+                                                       status);
+  else if (km == 4)
+    combine_kernel<T, 4><<<g, kCombineThreads, 0, s>>>(y_perm, D.d, row_of, gate, x, D.T, D.k, D.R_max, D.flags, y,
+                                                       status);
+  else
+    combine_kernel<T, 8><<<g, kCombineThreads, 0, s>>>(y_perm, D.d, row_of, gate, x, D.T, D.k, D.R_max, D.flags, y,
+                                                       status);
+  return cudaGetLastError();
+}
+}  // namespace
+
 cudaError_t launch_combine(const Dims &D, const float *y_perm, const float *y_split, int nsplit,
                            const int32_t *row_of, const float *gate, const void *x, void *y, int32_t *status,
                            cudaStream_t s) {
-  const unsigned g = grid_for(D.T, kWarps);
   if (!y_split) nsplit = 0;
+  if (nsplit > 7 || D.k > 8) return cudaErrorNotSupported;
+  if (D.T == 0) return cudaSuccess;
   if (D.dt == MOE_DT_BF16)
-    combine_kernel<__nv_bfloat16><<<g, kWarps * 32, 0, s>>>(y_perm, y_split, nsplit, D.d, row_of, gate,
-                                                            (const __nv_bfloat16 *)x, D.T, D.k, D.R_max, D.flags,
-                                                            (__nv_bfloat16 *)y, status);
-  else
-    combine_kernel<float><<<g, kWarps * 32, 0, s>>>(y_perm, y_split, nsplit, D.d, row_of, gate, (const float *)x,
-                                                    D.T, D.k, D.R_max, D.flags, (float *)y, status);
-  return cudaGetLastError();
+    return launch_combine_t<__nv_bfloat16>(D, y_perm, y_split, nsplit, row_of, gate, (const __nv_bfloat16 *)x,
+                                           (__nv_bfloat16 *)y, status, s);
+  return launch_combine_t<float>(D, y_perm, y_split, nsplit, row_of, gate, (const float *)x, (float *)y, status, s);
 }
 
 }  // namespace moe

@@ -86,12 +86,14 @@ __device__ __forceinline__ float reduce_scatter16(float (&v)[16], int lane) {
 // Each pass first issues the loads of kBatch vectors of both token rows (so
 // that many bytes are in flight per lane), then walks the expert rows (L1).
 constexpr int kBatch = 4;
+// x0, x1 and w_g point at the first column of a slice of len columns; d is
+// the row stride of W_g.
 template <typename T>
 __device__ __forceinline__ void chunk_logits(const T *__restrict__ x0, const T *__restrict__ x1, bool has1,
-                                             const T *__restrict__ w_g, int d, int N, int e0, int lane,
+                                             const T *__restrict__ w_g, int d, int len, int N, int e0, int lane,
                                              float (&acc)[16]) {
   constexpr int V = VecN<T>::n;
-  const int nvec = d / V;
+  const int nvec = len / V;
 #pragma unroll
   for (int i = 0; i < 16; ++i) acc[i] = 0.f;
   for (int vb = lane; vb < nvec; vb += 32 * kBatch) {
@@ -157,7 +159,7 @@ __global__ void __launch_bounds__(kWarps * 32) router_small_kernel(const T *__re
   if (t0 >= T_) return;
   const bool has1 = t0 + 1 < T_;
   float acc[16];
-  chunk_logits(x + t0 * d, x + (t0 + 1) * d, has1, w, d, N, 0, lane, acc);
+  chunk_logits(x + t0 * d, x + (t0 + 1) * d, has1, w, d, d, N, 0, lane, acc);
   float l = reduce_scatter16(acc, lane);
   const int e = (lane >> 1) & 7;
   const int64_t t = t0 + (lane >> 4);
@@ -207,6 +209,75 @@ __global__ void __launch_bounds__(kWarps * 32) router_small_kernel(const T *__re
   }
 }
 
+// Softmax, top-k and renormalisation of one token by one warp: lane L holds
+// the logits of experts L, L+32, ... (no bias yet) in lv. Ties go to the lower
+// expert; the picks are written in rank order.
+__device__ __forceinline__ void finish_token(float (&lv)[8], const float *__restrict__ router_bias, int N, int k,
+                                             int lane, int64_t t, int32_t *__restrict__ topk_idx,
+                                             float *__restrict__ gate, float *__restrict__ score) {
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    if (e < N) {
+      if (router_bias) lv[i] += router_bias[e];
+      m = fmaxf(m, lv[i]);
+    } else {
+      lv[i] = -INFINITY;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (lane + 32 * i < N) s += expf(lv[i] - m);
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
+  uint32_t taken = 0;
+  float sel_ex[8];
+  int sel_e[8];
+  float sel_sum = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j < k) {
+      float bv = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = lane + 32 * i;
+        if (e < N && !(taken & (1u << i)) && (lv[i] > bv || (lv[i] == bv && e < be))) {
+          bv = lv[i];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        const float ov = __shfl_xor_sync(kFull, bv, off);
+        const int oe = __shfl_xor_sync(kFull, be, off);
+        if (ov > bv || (ov == bv && oe < be)) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      sel_e[j] = be;
+      sel_ex[j] = expf(bv - m);
+      sel_sum += sel_ex[j];
+    }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < k) {
+        topk_idx[t * k + j] = sel_e[j];
+        score[t * k + j] = sel_ex[j] / s;
+        gate[t * k + j] = sel_ex[j] / sel_sum;
+      }
+    }
+  }
+}
+
 // Any N <= 256: chunk logits through shared memory.
 template <typename T>
 __global__ void __launch_bounds__(kWarps * 32) router_kernel(const T *__restrict__ x, const T *__restrict__ w_g,
@@ -221,7 +292,7 @@ __global__ void __launch_bounds__(kWarps * 32) router_kernel(const T *__restrict
   float *my = s_logits + warp * kTokPerWarp * N;
   for (int e0 = 0; e0 < N; e0 += kEC) {
     float acc[16];
-    chunk_logits(x + t0 * d, x + (t0 + 1) * d, has1, w_g, d, N, e0, lane, acc);
+    chunk_logits(x + t0 * d, x + (t0 + 1) * d, has1, w_g, d, d, N, e0, lane, acc);
     const float r = reduce_scatter16(acc, lane);
     const int e = e0 + ((lane >> 1) & 7);
     if ((lane & 1) == 0 && e < N) my[(lane >> 4) * N + e] = r;
@@ -232,66 +303,55 @@ __global__ void __launch_bounds__(kWarps * 32) router_kernel(const T *__restrict
     if (t >= T_) break;
     const float *L = my + tk * N;
     float lv[8];
-    float m = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      lv[i] = -INFINITY;
-      if (e < N) {
-        lv[i] = L[e];
-        if (router_bias) lv[i] += router_bias[e];
-        m = fmaxf(m, lv[i]);
+    for (int i = 0; i < 8; ++i) lv[i] = lane + 32 * i < N ? L[lane + 32 * i] : -INFINITY;
+    finish_token(lv, router_bias, N, k, lane, t, topk_idx, gate, score);
+  }
+}
+
+// Small batches: one CTA per pair of tokens, the 8 warps splitting d. Each
+// warp forms the partial logits of both tokens over its slice of columns
+// (8 experts at a time), the partials meet in shared memory and are summed in
+// warp order (deterministic), and warps 0 and 1 finish one token each. The
+// many CTAs keep enough bytes of x in flight even when T is a few dozen.
+template <typename T>
+__global__ void __launch_bounds__(kWarps * 32) router_split_kernel(const T *__restrict__ x,
+                                                                   const T *__restrict__ w_g,
+                                                                   const float *__restrict__ router_bias,
+                                                                   int64_t T_, int d, int N, int k,
+                                                                   int32_t *__restrict__ topk_idx,
+                                                                   float *__restrict__ gate,
+                                                                   float *__restrict__ score) {
+  extern __shared__ float s_part[];  // [kWarps][kTokPerWarp][N]
+  constexpr int V = VecN<T>::n;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t t0 = (int64_t)blockIdx.x * kTokPerWarp;
+  const bool has1 = t0 + 1 < T_;
+  const int nv = d / V;
+  const int v0 = warp * nv / kWarps, v1 = (warp + 1) * nv / kWarps;
+  const int c0 = v0 * V, len = (v1 - v0) * V;
+  float *my = s_part + warp * kTokPerWarp * N;
+  for (int e0 = 0; e0 < N; e0 += kEC) {
+    float acc[16];
+    chunk_logits(x + t0 * d + c0, x + (t0 + 1) * d + c0, has1, w_g + c0, d, len, N, e0, lane, acc);
+    const float r = reduce_scatter16(acc, lane);
+    const int e = e0 + ((lane >> 1) & 7);
+    if ((lane & 1) == 0 && e < N) my[(lane >> 4) * N + e] = r;
+  }
+  __syncthreads();
+  if (warp < kTokPerWarp) {
+    const int64_t t = t0 + warp;
+    if (t < T_) {
+      float lv[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = lane + 32 * i;
+        float v = 0.f;
+        if (e < N)
+          for (int w = 0; w < kWarps; ++w) v += s_part[(w * kTokPerWarp + warp) * N + e];
+        lv[i] = v;
       }
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
-    float s = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (lane + 32 * i < N) s += expf(lv[i] - m);
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
-    uint32_t taken = 0;
-    float sel_ex[8];
-    int sel_e[8];
-    float sel_sum = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (j < k) {
-        float bv = -INFINITY;
-        int be = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int e = lane + 32 * i;
-          if (e < N && !(taken & (1u << i)) && (lv[i] > bv || (lv[i] == bv && e < be))) {
-            bv = lv[i];
-            be = e;
-          }
-        }
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) {
-          const float ov = __shfl_xor_sync(kFull, bv, off);
-          const int oe = __shfl_xor_sync(kFull, be, off);
-          if (ov > bv || (ov == bv && oe < be)) {
-            bv = ov;
-            be = oe;
-          }
-        }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
-        sel_e[j] = be;
-        sel_ex[j] = expf(bv - m);
-        sel_sum += sel_ex[j];
-      }
-    }
-    if (lane == 0) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (j < k) {
-          topk_idx[t * k + j] = sel_e[j];
-          score[t * k + j] = sel_ex[j] / s;
-          gate[t * k + j] = sel_ex[j] / sel_sum;
-        }
-      }
+      finish_token(lv, router_bias, N, k, lane, t, topk_idx, gate, score);
     }
   }
 }
@@ -301,8 +361,20 @@ __global__ void __launch_bounds__(kWarps * 32) router_kernel(const T *__restrict
 cudaError_t launch_router(const Dims &D, const void *x, const void *w_g, const float *router_bias,
                           int32_t *topk_idx, float *gate, float *score, int32_t *status, cudaStream_t s) {
   (void)status;
-  const unsigned grid = (unsigned)((D.T + kTokPerBlock - 1) / kTokPerBlock);
   const bool bf16 = D.dt == MOE_DT_BF16;
+  if (router_split(D)) {
+    const unsigned g = (unsigned)((D.T + kTokPerWarp - 1) / kTokPerWarp);
+    const size_t smem = sizeof(float) * kWarps * kTokPerWarp * D.N;
+    if (bf16)
+      router_split_kernel<__nv_bfloat16><<<g, kWarps * 32, smem, s>>>(
+          (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)w_g, router_bias, D.T, (int)D.d, D.N, D.k, topk_idx,
+          gate, score);
+    else
+      router_split_kernel<float><<<g, kWarps * 32, smem, s>>>((const float *)x, (const float *)w_g, router_bias,
+                                                              D.T, (int)D.d, D.N, D.k, topk_idx, gate, score);
+    return cudaGetLastError();
+  }
+  const unsigned grid = (unsigned)((D.T + kTokPerBlock - 1) / kTokPerBlock);
   if (D.N <= kEC) {
     const size_t wbytes = (size_t)D.N * D.d * (bf16 ? 2 : 4);
     const bool stage = wbytes <= kMaxStagedW;

@@ -235,7 +235,14 @@ class Workspace:
             offsets=self.view("offsets", torch.int32, (N + 1,)), row_of=self.view("row_of", torch.int32, (T, k)),
             row_token=self.view("row_token", torch.int32, (R,)), row_gate=self.view("row_gate", torch.float32, (R,)),
             x_perm=self.view("x_perm", dt, (R, c.d)), h=self.view("h", dt, (R, c.d_ff)),
-            y_perm=self.view("y_perm", torch.float32, (R, c.d)))
+            y_perm=self.view("y_perm", torch.float32, (R, c.d)),
+            y_split=self.view("y_split", torch.float32, (self.splits - 1, R, c.d)))
+
+    @property
+    def splits(self):
+        """K slices of the decode-mode second GEMM (1 outside decode mode)."""
+        L = self.layout
+        return 1 + (L.ffn_sync - L.y_split) // (L.rows * self.cfg.d * 4)
 
     def status(self, stream=None):
         moe_get_device_status(self.buf, stream)

@@ -64,18 +64,24 @@ def test_permute_is_an_exact_gather(w):
     assert torch.all(xp[:rows][~used] == 0)
 
 
-@pytest.mark.parametrize("w", STAGE_CASES[:3], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", STAGE_CASES[:3] + [custom(64, 1024, 4096, 8, 2, math.inf, seed=13)],
+                         ids=lambda w: w.name)
 def test_combine_is_the_fixed_order_fp32_sum(w):
     """y[t] = sum over kept picks in pick order of y_perm rows, in fp32, then
     rounded once to the storage dtype: reproduced bit for bit."""
     inp = draw(w)
     g = parity.run_gpu(w, inp)
-    yp = g["_ws"].views()["y_perm"].cpu().numpy()
+    v = g["_ws"].views()
+    yp = v["y_perm"].cpu().numpy()
+    ys = v["y_split"].cpu().numpy()
     acc = np.zeros((w.T, w.d), dtype=np.float32)
     for j in range(w.k):
         r = g["row_of"][:, j]
         m = r >= 0
-        acc[m] = acc[m] + yp[r[m]]
+        term = yp[r[m]]
+        for sl in range(ys.shape[0]):
+            term = term + ys[sl][r[m]]
+        acc[m] = acc[m] + term
     ref = torch.from_numpy(acc).to(g["_y"].dtype)
     assert torch.equal(g["_y"].cpu(), ref)
 
@@ -158,6 +164,12 @@ E2E_CASES = [
     custom(640, 128, 128, 8, 2, 0.01, seed=10),  # tiny capacity: nearly everything dropped
     custom(333, 64, 128, 8, 2, 1.25, router_bias="const:3:-60", seed=11),  # an expert nobody picks
     custom(256, 64, 256, 4, 1, 1.25, dtype="f32", router_bias="zipf", seed=12),  # fp32 with drops
+] + [
+    # decode-shaped batches (bf16, T*k <= 64*N): swap-AB expert GEMMs, second GEMM split along d_ff
+    custom(64, 1024, 4096, 8, 2, math.inf, seed=13),
+    custom(48, 512, 2048, 8, 2, 1.0, router_bias="zipf", seed=14),  # drops
+    custom(5, 768, 3072, 16, 4, math.inf, seed=15),  # fewer picks than experts
+    custom(40, 520, 1000, 8, 2, 1.25, seed=16),  # ragged d and d_ff: partial k-blocks and weight tiles
 ]
 
 
