@@ -30,6 +30,10 @@
  *     on the host and returned before anything is enqueued. Errors found by
  *     kernels (a wait that timed out, an index out of bounds) are recorded in
  *     the workspace's status word and read with moe_get_device_status.
+ *   - Kernels are launched with programmatic stream serialisation: a kernel
+ *     may be scheduled while the previous kernel on the stream finishes, but
+ *     waits for that kernel's completion before it touches global memory, so
+ *     stream order holds as usual.
  *   - Every entry point returns a moe_status; moe_last_error() gives the text
  *     of the last failure on the calling thread. Nothing throws across the ABI.
  *   - Limits: T >= 1, T*k < 2^31; 1 <= N <= 256; 1 <= k <= min(N, 8);
@@ -108,7 +112,10 @@ typedef struct {
   size_t h;           /* dtype [rows, d_ff] expert hidden activations */
   size_t y_perm;      /* fp32  [rows, d]    gate-scaled expert outputs */
   size_t y_split;     /* fp32  [S-1, rows, d] decode-shaped configs only: the second GEMM's extra K slices */
-  size_t ffn_sync;    /* int32 [N] decode-shaped configs only: per-expert count of stored h tiles */
+  size_t ffn_sync;    /* int32 bf16 configs: completion counters of h tiles (per expert in decode-shaped
+                       * configs, else per 256-row block) and an exit count, read by the fused expert
+                       * FFN; zero between calls (moe_workspace_init, moe_dispatch and every
+                       * completed moe_expert_ffn leave them zero) */
   size_t total;       /* bytes of the whole workspace */
   int64_t rows;       /* R_max */
   int64_t capacity;   /* C */
@@ -132,8 +139,9 @@ moe_status moe_get_workspace_layout(const moe_config *cfg, moe_workspace_layout 
 /* Bytes of workspace moe_forward needs for cfg (0 for an invalid config). */
 size_t moe_workspace_bytes(const moe_config *cfg);
 
-/* Clear the status word of a workspace. Call once after allocating it (the
- * word is sticky: later calls never clear it). Enqueued on stream. */
+/* Clear the status word and the expert FFN's completion counters of a
+ * workspace. Call once after allocating it (the status word is sticky: later
+ * calls never clear it). Enqueued on stream. */
 moe_status moe_workspace_init(const moe_config *cfg, void *ws, moe_stream_t stream);
 
 /* Wait for stream, then return the workspace's device status: MOE_OK, or the
@@ -174,10 +182,10 @@ moe_status moe_dispatch(const moe_config *cfg, const void *x, const int32_t *top
  *   tcgen05, accumulating in tensor memory). For decode-shaped configs (bf16,
  *   T*k <= 64*N) the second GEMM is split along d_ff: y_perm receives the
  *   first slice and the workspace's y_split the others, which moe_combine
- *   (given the same workspace) adds in slice order; both GEMMs then run in
- *   one launch, whose second-GEMM tiles wait (bounded, MOE_ERR_TIMEOUT) on
- *   per-expert counters in the workspace's ffn_sync, reset on the stream
- *   before each launch. */
+ *   (given the same workspace) adds in slice order. For bf16 configs both
+ *   GEMMs run in one launch, whose second-GEMM tiles wait (bounded,
+ *   MOE_ERR_TIMEOUT) on completion counters in the workspace's ffn_sync
+ *   (zero on entry; the launch's last CTA leaves them zero). */
 moe_status moe_expert_ffn(const moe_config *cfg, const void *x_perm, const int32_t *offsets, const void *w1,
                           const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
                           float *y_perm, void *ws, moe_stream_t stream);

@@ -98,7 +98,12 @@ template <bool kResident>
 __global__ void __launch_bounds__(kThreads) capacity_kernel(
     const int32_t *__restrict__ idx, const float *__restrict__ gate, const float *__restrict__ score, int64_t n,
     int k, int N, int64_t C, int align, int32_t *counts_raw, int32_t *counts_kept, int32_t *offsets,
-    int32_t *row_of, int32_t *row_token, float *row_gate, int64_t R_max, int32_t *status) {
+    int32_t *row_of, int32_t *row_token, float *row_gate, int64_t R_max, int32_t *ffn_sync, int n_sync,
+    int32_t *status) {
+  pdl_wait();
+  // the expert FFN's completion counters start every forward at zero
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < n_sync; i += kThreads) ffn_sync[i] = 0;
   extern __shared__ int s_hist[];  // [kWarps][N]
   __shared__ int s_warp[32];
   __shared__ int s_sel[256];
@@ -270,20 +275,16 @@ __global__ void __launch_bounds__(kThreads) capacity_kernel(
 cudaError_t launch_capacity(const Dims &D, const int32_t *topk_idx, const float *gate, const float *score,
                             int32_t *counts_raw, int32_t *counts_kept, int32_t *offsets, uint32_t *sel_thr,
                             int32_t *sel_eq, int32_t *row_of, int32_t *row_token, float *row_gate,
-                            int32_t *status, cudaStream_t s) {
+                            int32_t *ffn_sync, int32_t *status, cudaStream_t s) {
   (void)sel_thr;
   (void)sel_eq;
   const int64_t n = D.T * D.k;
   const size_t smem = sizeof(int) * kWarps * D.N;
-  if (n <= (int64_t)kThreads * kItems)
-    capacity_kernel<true><<<D.N, kThreads, smem, s>>>(topk_idx, gate, score, n, D.k, D.N, D.C, row_align(D),
-                                                      counts_raw, counts_kept, offsets, row_of, row_token, row_gate,
-                                                      D.R_max, status);
-  else
-    capacity_kernel<false><<<D.N, kThreads, smem, s>>>(topk_idx, gate, score, n, D.k, D.N, D.C, row_align(D),
-                                                       counts_raw, counts_kept, offsets, row_of, row_token, row_gate,
-                                                       D.R_max, status);
-  return cudaGetLastError();
+  const int n_sync = ffn_sync ? (int)ffn_sync_ints(D) : 0;
+  auto kern = n <= (int64_t)kThreads * kItems ? capacity_kernel<true> : capacity_kernel<false>;
+  return launch_k(kern, dim3(D.N), dim3(kThreads), smem, s, 1u, topk_idx, gate, score, n, D.k, D.N, D.C,
+                  row_align(D), counts_raw, counts_kept, offsets, row_of, row_token, row_gate, D.R_max, ffn_sync,
+                  n_sync, status);
 }
 
 }  // namespace moe

@@ -21,6 +21,7 @@ __global__ void __launch_bounds__(256) ffn_simt_kernel(const Tin *__restrict__ A
                                                        int64_t N_out, const float *__restrict__ row_gate,
                                                        const int32_t *__restrict__ offsets, int N_exp,
                                                        Tout *__restrict__ out) {
+  pdl_wait();
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[BK][BN + 4];
   const int64_t m0 = (int64_t)blockIdx.y * BM;
@@ -83,27 +84,18 @@ cudaError_t launch_ffn_simt(const Dims &D, int epi, const void *A, int64_t K, co
                             int64_t N_out, const float *row_gate, const int32_t *offsets, void *out,
                             int32_t *status, cudaStream_t s) {
   (void)status;
-  dim3 grid((unsigned)((N_out + BN - 1) / BN), (unsigned)(D.R_max / BM));
-  if (D.dt == MOE_DT_F32) {
-    if (epi == 1)
-      ffn_simt_kernel<float, float, 1><<<grid, 256, 0, s>>>((const float *)A, K, (const float *)B,
-                                                            (const float *)bias, N_out, row_gate, offsets, D.N,
-                                                            (float *)out);
-    else
-      ffn_simt_kernel<float, float, 2><<<grid, 256, 0, s>>>((const float *)A, K, (const float *)B,
-                                                            (const float *)bias, N_out, row_gate, offsets, D.N,
-                                                            (float *)out);
-  } else {
-    if (epi == 1)
-      ffn_simt_kernel<__nv_bfloat16, __nv_bfloat16, 1><<<grid, 256, 0, s>>>(
-          (const __nv_bfloat16 *)A, K, (const __nv_bfloat16 *)B, (const __nv_bfloat16 *)bias, N_out, row_gate,
-          offsets, D.N, (__nv_bfloat16 *)out);
-    else
-      ffn_simt_kernel<__nv_bfloat16, float, 2><<<grid, 256, 0, s>>>(
-          (const __nv_bfloat16 *)A, K, (const __nv_bfloat16 *)B, (const __nv_bfloat16 *)bias, N_out, row_gate,
-          offsets, D.N, (float *)out);
-  }
-  return cudaGetLastError();
+  const dim3 grid((unsigned)((N_out + BN - 1) / BN), (unsigned)(D.R_max / BM));
+  if (D.dt == MOE_DT_F32)
+    return launch_k(epi == 1 ? ffn_simt_kernel<float, float, 1> : ffn_simt_kernel<float, float, 2>, grid, dim3(256),
+                    0, s, 1u, (const float *)A, K, (const float *)B, (const float *)bias, N_out, row_gate, offsets,
+                    D.N, (float *)out);
+  if (epi == 1)
+    return launch_k(ffn_simt_kernel<__nv_bfloat16, __nv_bfloat16, 1>, grid, dim3(256), 0, s, 1u,
+                    (const __nv_bfloat16 *)A, K, (const __nv_bfloat16 *)B, (const __nv_bfloat16 *)bias, N_out,
+                    row_gate, offsets, D.N, (__nv_bfloat16 *)out);
+  return launch_k(ffn_simt_kernel<__nv_bfloat16, float, 2>, grid, dim3(256), 0, s, 1u, (const __nv_bfloat16 *)A, K,
+                  (const __nv_bfloat16 *)B, (const __nv_bfloat16 *)bias, N_out, row_gate, offsets, D.N,
+                  (float *)out);
 }
 
 }  // namespace moe

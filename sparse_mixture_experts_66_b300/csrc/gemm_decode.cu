@@ -85,18 +85,6 @@ __device__ __forceinline__ DTile decode_tile(const DCtrl *c, int N_exp, int m1, 
   return d;
 }
 
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-__device__ __forceinline__ void red_release_add(int32_t *p, int v) {
-  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ int ld_acquire(const int32_t *p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
 __global__ void __launch_bounds__(kDThreads, 1)
     ffn_decode_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_x,
                       const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_h,
@@ -115,6 +103,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
   const int kb1_count = (d + kDBK - 1) / kDBK, kb2_count = (d_ff + kDBK - 1) / kDBK;
 
   if (warp == 0) {
+    pdl_wait();  // offsets come from the dispatch
     int n1[8], n2[8];
     int s1 = 0, s2 = 0;
     bool bad = false;
@@ -187,6 +176,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();
   const int total = c->total2;
   const uint32_t tmem = c->tmem_base;
 
@@ -204,21 +194,9 @@ __global__ void __launch_bounds__(kDThreads, 1)
           kb1 = (tl.sp + 1) * kb2_count / S;
           // every GEMM1 tile of this expert must have stored its rows of h
           const int need = (c->offsets[tl.e + 1] - c->offsets[tl.e]) / kDN * m1 * 4;
-          if (ld_acquire(h_done + tl.e) < need) {
-            const unsigned long long ts = globaltimer();
-            while (ld_acquire(h_done + tl.e) < need) {
-              if (*abort) {
-                ok = false;
-                break;
-              }
-              if (globaltimer() - ts > kTimeoutNs) {
-                report_error(status, MOE_ERR_TIMEOUT, kKGemmTcDecode, 5);
-                *abort = 1;
-                ok = false;
-                break;
-              }
-            }
-            if (!ok) break;
+          if (!wait_counter(h_done + tl.e, need, abort, status, kKGemmTcDecode, 5)) {
+            ok = false;
+            break;
           }
           fence_proxy_async_global();
         }
@@ -307,37 +285,45 @@ __global__ void __launch_bounds__(kDThreads, 1)
     uint32_t aph = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const DTile tl = decode_tile(c, N_exp, m1, m2, S, t);
-      int ok = 0;
-      if (lane == 0) ok = mbar_wait(&c->tfull[acc], aph, abort, status, kKGemmTcDecode, 40 + acc) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      tc_fence_after();
+      // the bias and the chunk's row gates are fetched before the accumulator
+      // wait, so no load latency sits between TMEM and the stores
       const int M_out = tl.phase ? d : d_ff;
       const int f = tl.m * kDM + q * 32 + lane;  // this thread's weight row (output feature)
       const bool fvalid = f < M_out;
       float b = 0.f;
       if (fvalid && (tl.phase == 0 || tl.sp == 0))
         b = __bfloat162float((tl.phase ? b2 : b1)[(int64_t)tl.e * M_out + f]);
+      float gate_lo = 1.0f, gate_hi = 1.0f;  // row gates of chunk rows lane and 32 + lane
+      if (tl.phase && row_gate) {
+        gate_lo = row_gate[tl.row0 + lane];
+        gate_hi = row_gate[tl.row0 + 32 + lane];
+      }
       float *dst = tl.phase ? (tl.sp == 0 ? y_perm : y_split + (int64_t)(tl.sp - 1) * R_max * d) : nullptr;
+      int ok = 0;
+      if (lane == 0) ok = mbar_wait(&c->tfull[acc], aph, abort, status, kKGemmTcDecode, 40 + acc) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
 #pragma unroll 1
       for (int c0 = 0; c0 < kDN; c0 += 32) {
         uint32_t r[32];
         __syncwarp();
         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kDN + c0), r);
-        if (fvalid) {
-          if (tl.phase == 0) {
+        if (tl.phase == 0) {
+          if (fvalid) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const int64_t row = (int64_t)tl.row0 + c0 + j;
               h[row * d_ff + f] = __float2bfloat16_rn(gelu_as(__uint_as_float(r[j]) + b));
             }
-          } else {
+          }
+        } else {
+          const float gsrc = c0 == 0 ? gate_lo : gate_hi;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int64_t row = (int64_t)tl.row0 + c0 + j;
-              const float g = row_gate ? row_gate[row] : 1.0f;
-              dst[row * d + f] = g * (__uint_as_float(r[j]) + b);
-            }
+          for (int j = 0; j < 32; ++j) {
+            const int64_t row = (int64_t)tl.row0 + c0 + j;
+            const float g = __shfl_sync(0xffffffffu, gsrc, j);
+            if (fvalid) dst[row * d + f] = g * (__uint_as_float(r[j]) + b);
           }
         }
       }
@@ -354,11 +340,21 @@ __global__ void __launch_bounds__(kDThreads, 1)
     }
   }
 
+  pdl_trigger();  // this CTA has no tiles left: the next kernel may launch
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * kDN));
+  }
+  // The last CTA out resets the expert counters (and the exit count) for the
+  // next launch: every other CTA has finished all its counter accesses.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(h_done + N_exp, 1) == (int)gridDim.x - 1) {
+      __threadfence();
+      for (int i = 0; i <= N_exp; ++i) h_done[i] = 0;
+    }
   }
 }
 
@@ -442,29 +438,16 @@ cudaError_t launch_ffn_decode(const Dims &D, const void *x_perm, const int32_t *
   if (!make_map(&tw1, w1, 3, dw1, kDM) || !make_map(&tx, x_perm, 2, dx, kDN) || !make_map(&tw2, w2, 3, dw2, kDM) ||
       !make_map(&th, h, 2, dh, kDN))
     return cudaErrorInvalidValue;
-  // h_done counts, per expert, the epilogue warps that finished a GEMM1 tile
-  cudaError_t e = cudaMemsetAsync(h_done, 0, sizeof(int32_t) * D.N, s);
-  if (e != cudaSuccess) return e;
   const int64_t chunks = D.R_max / kDN;
   const int64_t max_tiles = chunks * ((D.d_ff + kDM - 1) / kDM) + chunks * S * ((D.d + kDM - 1) / kDM);
   int grid = num_sms();
   if (max_tiles < grid) grid = (int)max_tiles;
   if (grid < 1) grid = 1;
-  // A cooperative launch: every CTA is resident at once, so a second-GEMM tile
-  // never waits on a first-GEMM tile of a CTA that has not started.
-  cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3((unsigned)grid);
-  lc.blockDim = dim3(kDThreads);
-  lc.dynamicSmemBytes = kDSmem;
-  lc.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  lc.attrs = attr;
-  lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, ffn_decode_kernel, tw1, tx, tw2, th, offsets, (int)D.N, (int64_t)D.R_max, (int)D.d,
-                            (int)D.d_ff, S, (const __nv_bfloat16 *)b1, (const __nv_bfloat16 *)b2, row_gate,
-                            (__nv_bfloat16 *)h, y_perm, y_split, h_done, status);
+  // One CTA per SM at most (shared memory) and no more CTAs than SMs, so all
+  // are resident together: a GEMM2 tile never waits on a CTA that cannot run.
+  return launch_k(ffn_decode_kernel, dim3((unsigned)grid), dim3(kDThreads), kDSmem, s, 1u, tw1, tx, tw2, th, offsets,
+                  (int)D.N, (int64_t)D.R_max, (int)D.d, (int)D.d_ff, S, (const __nv_bfloat16 *)b1,
+                  (const __nv_bfloat16 *)b2, row_gate, (__nv_bfloat16 *)h, y_perm, y_split, h_done, status);
 }
 
 }  // namespace moe

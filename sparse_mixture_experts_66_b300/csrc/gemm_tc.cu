@@ -13,10 +13,11 @@
 // rows, so each 128-row half tile belongs to one expert and uses one weight
 // matrix.
 //
-// Persistent kernel on CTA pairs (clusters of 2, one CTA per SM): each pair
-// walks 256 x 256 output tiles of all experts (expert by expert; inside an
-// expert n-tile by n-tile with the 256-row tiles fastest, so the expert's rows
-// stay in L2 while its weight tiles stream once). Warp roles in each CTA:
+// One persistent launch on CTA pairs (clusters of 2, one CTA per SM) for both
+// GEMMs: each pair walks 256 x 256 output tiles of all experts, first of
+// GEMM1 and then of GEMM2 (per GEMM expert by expert; inside an expert n-tile
+// by n-tile with the 256-row blocks fastest, so the expert's rows stay in L2
+// while its weight tiles stream once). Warp roles in each CTA:
 //   warp 0    TMA producer: this CTA's 128 rows of A and its half (128 rows)
 //             of the B tile per 64-deep k-block (128-byte swizzle), a ring of
 //             six 32 KB stages; completion is signalled on the leader's
@@ -42,8 +43,9 @@ using namespace tc;
 
 constexpr int BM = 128;
 constexpr int BK = 64;  // one 128-byte swizzle atom of bf16
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 8;  // a multiple of 4 (one group per TMEM lane quarter) dividing 32
 constexpr int kThreads = 64 + kEpiWarps * 32;
+static_assert(kEpiWarps % 4 == 0 && (256 / (kEpiWarps / 4)) % 32 == 0, "epilogue column split");
 constexpr int kMaxExperts = 256;
 
 
@@ -51,9 +53,12 @@ struct Ctrl {
   unsigned long long full[8], empty[8], tfull[2], tempty[2], drain;
   uint32_t tmem_base;
   int abort;
-  int total_tiles;
+  int total1, total;  // GEMM1 tiles; GEMM1 + GEMM2 tiles
   int32_t offsets[kMaxExperts + 1];
-  int32_t tile_start[kMaxExperts + 1];
+  int32_t blk_start[kMaxExperts + 1];  // first 256-row block of each expert
+  int32_t start1[kMaxExperts + 1];     // first GEMM1 tile of each expert
+  int32_t start2[kMaxExperts + 1];     // first GEMM2 tile of each expert (counted from total1)
+  uint4 bias[kEpiWarps][256 / (kEpiWarps / 4) / 8];  // each epilogue warp's bias columns of its current tile
 };
 
 
@@ -121,6 +126,16 @@ __device__ __forceinline__ void umma_commit_pair(unsigned long long *bar, uint16
 // barrier; MMA commits are multicast to both CTAs; the peer's epilogue warps
 // arrive remotely on the leader's TMEM-empty barrier.
 //
+// One launch runs both GEMMs: the tile list holds every GEMM1 tile and then
+// every GEMM2 tile, dealt round-robin to the pairs, so GEMM2 tiles start
+// while the last GEMM1 tiles finish elsewhere and neither GEMM leaves a
+// partly idle last wave. A GEMM2 tile of a 256-row block waits (bounded) until
+// all GEMM1 tiles of that block have stored h: each of the 16 epilogue warps
+// of a GEMM1 tile fences its stores for the async proxy and adds 1 (release)
+// to the block's counter; the GEMM2 producers acquire it before loading h.
+// The order is deadlock-free with all pairs resident: a tile only waits on
+// tiles earlier in the list, and each pair walks its tiles in list order.
+//
 // Tiles: per expert, pair tiles of 256 rows (two 128-row segment tiles); when
 // an expert has an odd number of 128-row tiles, the peer's half of its last
 // pair tile lies past the segment and its rows are computed but not stored.
@@ -131,25 +146,41 @@ constexpr int kStageP = kAP + kBP;
 constexpr int BNP = 256;                  // pair tile width
 constexpr size_t kSmemP = 1024 + (size_t)kStagesP * kStageP + sizeof(Ctrl);
 
-__device__ __forceinline__ void decode_pair_tile(const Ctrl *c, int N_exp, int t, int &e, int &m0, int &n_idx) {
+struct PTile {
+  int phase;  // 0: GEMM1, 1: GEMM2
+  int e;      // expert
+  int m0;     // first row of the 256-row pair tile
+  int ni;     // n-tile
+  int blk;    // index of the 256-row block (dependency counter)
+};
+
+__device__ __forceinline__ PTile decode_pair_tile(const Ctrl *c, int N_exp, int t) {
+  PTile p;
+  p.phase = t >= c->total1 ? 1 : 0;
+  const int32_t *start = p.phase ? c->start2 : c->start1;
+  const int tt = p.phase ? t - c->total1 : t;
   int lo = 0, hi = N_exp - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (c->tile_start[mid] <= t) lo = mid; else hi = mid - 1;
+    if (start[mid] <= tt) lo = mid; else hi = mid - 1;
   }
-  e = lo;
-  const int mp = ((c->offsets[e + 1] - c->offsets[e]) / BM + 1) / 2;
-  const int local = t - c->tile_start[e];
-  n_idx = local / mp;
-  m0 = c->offsets[e] + (local - n_idx * mp) * (2 * BM);
+  p.e = lo;
+  const int mp = c->blk_start[lo + 1] - c->blk_start[lo];
+  const int local = tt - start[lo];
+  p.ni = local / mp;
+  const int pb = local - p.ni * mp;
+  p.m0 = c->offsets[lo] + pb * (2 * BM);
+  p.blk = c->blk_start[lo] + pb;
+  return p;
 }
 
-template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                     const int32_t *__restrict__ offsets_g, int N_exp, int64_t R_max, int K, int N_out,
-                     const __nv_bfloat16 *__restrict__ bias, const float *__restrict__ row_gate,
-                     void *__restrict__ out, int32_t *status) {
+    ffn_pair_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w1,
+                    const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w2,
+                    const int32_t *__restrict__ offsets_g, int N_exp, int64_t R_max, int d, int d_ff,
+                    const __nv_bfloat16 *__restrict__ b1, const __nv_bfloat16 *__restrict__ b2,
+                    const float *__restrict__ row_gate, __nv_bfloat16 *__restrict__ h, float *__restrict__ y_perm,
+                    int32_t *__restrict__ blk_done, int nblk_max, int32_t *status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t *sA = base;
@@ -160,23 +191,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-  const int n_tiles = (N_out + BNP - 1) / BNP;
-  const int kb_count = (K + BK - 1) / BK;
+  const int n1 = (d_ff + BNP - 1) / BNP, n2 = (d + BNP - 1) / BNP;
+  const int kb1 = (d + BK - 1) / BK, kb2 = (d_ff + BK - 1) / BK;
+  const int need = n1 * 2 * kEpiWarps;  // epilogue-warp arrivals that complete a 256-row block of h
 
   if (warp == 0) {
-    int local[8];
+    pdl_wait();  // offsets come from the dispatch
+    int nb[8];
     int sum = 0;
     bool bad = false;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int e = lane * 8 + i;
-      local[i] = 0;
+      nb[i] = 0;
       if (e < N_exp) {
         const int o0 = offsets_g[e], o1 = offsets_g[e + 1];
         if (o1 < o0 || (o1 - o0) % BM != 0 || o1 > R_max) bad = true;
-        else local[i] = ((o1 - o0) / BM + 1) / 2 * n_tiles;
+        else nb[i] = ((o1 - o0) / BM + 1) / 2;
       }
-      sum += local[i];
+      sum += nb[i];
     }
     bad = __any_sync(0xffffffffu, bad);
     int incl = sum;
@@ -190,16 +223,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 8; ++i) {
       const int e = lane * 8 + i;
       if (e < N_exp) {
-        c->tile_start[e] = excl;
+        c->blk_start[e] = excl;
+        c->start1[e] = excl * n1;
+        c->start2[e] = excl * n2;
         c->offsets[e] = offsets_g[e];
       }
-      excl += local[i];
+      excl += nb[i];
     }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    const int blocks = __shfl_sync(0xffffffffu, incl, 31);
     if (lane == 0) {
       c->offsets[N_exp] = offsets_g[N_exp];
-      c->tile_start[N_exp] = total;
-      c->total_tiles = bad ? 0 : total;
+      c->blk_start[N_exp] = blocks;
+      c->start1[N_exp] = blocks * n1;
+      c->start2[N_exp] = blocks * n2;
+      c->total1 = bad ? 0 : blocks * n1;
+      c->total = bad ? 0 : blocks * (n1 + n2);
       c->abort = 0;
       if (bad && rank == 0) report_error(status, MOE_ERR_BOUNDS, kKGemmTc, 2);
     }
@@ -225,8 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   cluster_sync_all();  // the peer's barriers are initialised before anyone signals them
   tc_fence_after();
+  pdl_wait();
 
-  const int total = c->total_tiles;
+  const int total = c->total;
   const uint32_t tmem = c->tmem_base;
 
   if (warp == 0) {
@@ -238,18 +277,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the leader's full barriers: consecutive 8-byte objects, mapped once
       const uint32_t full_leader0 = map_to_rank(saddr(&c->full[0]), 0);
       for (int t = pair; ok && t < total; t += npairs) {
-        int e, m0, ni;
-        decode_pair_tile(c, N_exp, t, e, m0, ni);
-        const int a_row = m0 + (int)rank * BM, b_row = ni * BNP + (int)rank * 128;
-        for (int kb = 0; kb < kb_count; ++kb) {
+        const PTile tl = decode_pair_tile(c, N_exp, t);
+        const int a_row = tl.m0 + (int)rank * BM, b_row = tl.ni * BNP + (int)rank * 128;
+        const CUtensorMap *ma = tl.phase ? &tm_h : &tm_x;
+        const CUtensorMap *mb = tl.phase ? &tm_w2 : &tm_w1;
+        const int kbn = tl.phase ? kb2 : kb1;
+        if (tl.phase) {
+          if (!wait_counter(blk_done + tl.blk, need, abort, status, kKGemmTc, 3)) break;
+          fence_proxy_async_global();
+        }
+        for (int kb = 0; kb < kbn; ++kb) {
           if (!mbar_wait_fast(&c->empty[s], ph ^ 1u, abort, status, kKGemmTc, 50 + s)) {
             ok = false;
             break;
           }
           if (rank == 0) mbar_expect_tx(&c->full[s], 2 * kStageP);
           const uint32_t full_leader = full_leader0 + 8u * (uint32_t)s;
-          tma_load_2d_pair(sA + s * kAP, &tm_a, full_leader, kb * BK, a_row);
-          tma_load_3d_pair(sB + s * kBP, &tm_b, full_leader, kb * BK, b_row, e);
+          tma_load_2d_pair(sA + s * kAP, ma, full_leader, kb * BK, a_row);
+          tma_load_3d_pair(sB + s * kBP, mb, full_leader, kb * BK, b_row, tl.e);
           issued_mask |= 1u << s;
           parity_mask = (parity_mask & ~(1u << s)) | (ph << s);
           if (++s == kStagesP) {
@@ -258,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!ok && rank == 0) {  // the leader's full barriers track both CTAs' copies: drain them
+      if (*abort && rank == 0) {  // the leader's full barriers track both CTAs' copies: drain them
         for (int i = 0; i < kStagesP; ++i)
           if (issued_mask & (1u << i)) {
             const unsigned long long t0 = globaltimer();
@@ -280,10 +325,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 14-bit address field below 256 KB)
       const uint64_t adesc0 = smem_desc_sw128(saddr(sA)), bdesc0 = smem_desc_sw128(saddr(sB));
       for (int t = pair; ok && t < total; t += npairs) {
+        const int kbn = t >= c->total1 ? kb2 : kb1;
         if (!mbar_wait_fast(&c->tempty[acc], aph ^ 1u, abort, status, kKGemmTc, 60 + acc)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + (uint32_t)(acc * BNP);
-        for (int kb = 0; kb < kb_count; ++kb) {
+        for (int kb = 0; kb < kbn; ++kb) {
           if (!mbar_wait_fast(&c->full[s], ph, abort, status, kKGemmTc, 70 + s)) {
             ok = false;
             break;
@@ -314,35 +360,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     const int q = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int part = (warp - 2) >> 2;  // which share of the tile's columns (warps per lane quarter split them)
+    constexpr int kCols = BNP / (kEpiWarps / 4);
     const int row_in_tile = (int)rank * BM + q * 32 + lane;
     const uint32_t tempty_leader0 = map_to_rank(saddr(&c->tempty[0]), 0);
     const uint32_t tempty_leader1 = map_to_rank(saddr(&c->tempty[1]), 0);
     int acc = 0;
     uint32_t aph = 0;
+    uint4 *sbias = c->bias[warp - 2];
     for (int t = pair; t < total; t += npairs) {
-      int e, m0, ni;
-      decode_pair_tile(c, N_exp, t, e, m0, ni);
+      const PTile tl = decode_pair_tile(c, N_exp, t);
+      // everything the tile's epilogue reads from memory is fetched before the
+      // accumulator wait, so no load latency sits between TMEM and the stores
+      const int64_t row = (int64_t)tl.m0 + row_in_tile;
+      const bool valid = row < c->offsets[tl.e + 1];
+      const int N_out = tl.phase ? d : d_ff;
+      const float g = (tl.phase && row_gate && valid) ? row_gate[row] : 1.0f;
+      {
+        const __nv_bfloat16 *bias = tl.phase ? b2 : b1;
+        const int nb = tl.ni * BNP + part * kCols + lane * 8;
+        __syncwarp();  // the previous tile's reads of sbias are done
+        if (lane < kCols / 8)
+          sbias[lane] = nb < N_out ? __ldg(reinterpret_cast<const uint4 *>(bias + (int64_t)tl.e * N_out + nb))
+                                   : make_uint4(0u, 0u, 0u, 0u);
+        __syncwarp();
+      }
       int ok = 0;
       if (lane == 0) ok = mbar_wait(&c->tfull[acc], aph, abort, status, kKGemmTc, 80 + acc) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const int64_t row = (int64_t)m0 + row_in_tile;
-      const bool valid = row < c->offsets[e + 1];
-      const float g = (EPI == 2 && row_gate && valid) ? row_gate[row] : 1.0f;
 #pragma unroll 1
-      for (int cc = 0; cc < BNP / 64; ++cc) {
-        const int col0 = half * (BNP / 2) + cc * 32;
+      for (int cc = 0; cc < kCols / 32; ++cc) {
+        const int col0 = part * kCols + cc * 32;
         uint32_t r[32];
         __syncwarp();  // the TMEM load is warp-collective: reconverge after the row-masked stores
         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BNP + col0), r);
-        const int n = ni * BNP + col0;
-        const __nv_bfloat16 *bp = bias + (int64_t)e * N_out + n;
+        const int n = tl.ni * BNP + col0;
 #pragma unroll
         for (int g8 = 0; g8 < 4; ++g8) {
-          if (!valid || n + g8 * 8 >= N_out) break;
-          const uint4 braw = __ldg(reinterpret_cast<const uint4 *>(bp + g8 * 8));
+          const bool store = valid && n + g8 * 8 < N_out;
+          const uint4 braw = sbias[cc * 4 + g8];
           const uint32_t bw[4] = {braw.x, braw.y, braw.z, braw.w};
           float v[8];
 #pragma unroll
@@ -350,33 +408,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             v[2 * j] = __uint_as_float(r[g8 * 8 + 2 * j]) + __uint_as_float(bw[j] << 16);
             v[2 * j + 1] = __uint_as_float(r[g8 * 8 + 2 * j + 1]) + __uint_as_float(bw[j] & 0xffff0000u);
           }
-          if (EPI == 1) {
+          if (tl.phase == 0) {
             uint32_t pk[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               __nv_bfloat162 h2 = __floats2bfloat162_rn(gelu_as(v[2 * j]), gelu_as(v[2 * j + 1]));
               pk[j] = *reinterpret_cast<uint32_t *>(&h2);
             }
-            __nv_bfloat16 *o = (__nv_bfloat16 *)out + row * N_out + n + g8 * 8;
-            *reinterpret_cast<uint4 *>(o) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          } else {
-            float *o = (float *)out + row * N_out + n + g8 * 8;
+            if (store) *reinterpret_cast<uint4 *>(h + row * d_ff + n + g8 * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          } else if (store) {
+            float *o = y_perm + row * d + n + g8 * 8;
             *reinterpret_cast<float4 *>(o) = make_float4(g * v[0], g * v[1], g * v[2], g * v[3]);
             *reinterpret_cast<float4 *>(o + 4) = make_float4(g * v[4], g * v[5], g * v[6], g * v[7]);
           }
         }
       }
+      if (tl.phase == 0) fence_proxy_async_global();  // h stores before the GEMM2 tiles' TMA loads
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         if (rank == 0) mbar_arrive(&c->tempty[acc]);
         else mbar_arrive_cluster(acc == 0 ? tempty_leader0 : tempty_leader1);
+        if (tl.phase == 0) red_release_add(blk_done + tl.blk, 1);
       }
       acc ^= 1;
       if (acc == 0) aph ^= 1u;
     }
   }
 
+  pdl_trigger();  // this CTA has no tiles left: the next kernel may launch
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();  // no CTA leaves while its peer may still signal its barriers
@@ -384,52 +444,73 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * BNP));
   }
+  // The last CTA out resets the block counters (and the exit count) for the
+  // next launch: every other CTA has finished all its counter accesses.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(blk_done + nblk_max, 1) == (int)gridDim.x - 1) {
+      __threadfence();
+      for (int i = 0; i < nblk_max; ++i) blk_done[i] = 0;
+      blk_done[nblk_max] = 0;
+    }
+  }
 }
 
-template <int EPI>
-cudaError_t launch_pair(const Dims &D, const void *A, int64_t K, const void *B, const void *bias, int64_t N_out,
-                        const float *row_gate, const int32_t *offsets, void *out, int32_t *status, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemP);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
+// Clusters of 2 that can be resident at once (every pair must be, for the
+// GEMM2 tiles' waits to end).
+int resident_pairs() {
+  static int n = 0;
+  if (!n) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 256);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemP;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, ffn_pair_kernel, &cfg) != cudaSuccess || clusters < 1) {
+      cudaGetLastError();
+      clusters = num_sms() / 2;
+    }
+    n = clusters < num_sms() / 2 ? clusters : num_sms() / 2;
   }
-  CUtensorMap ta, tb;
-  const uint64_t da[2] = {(uint64_t)K, (uint64_t)D.R_max};
-  const uint64_t db[3] = {(uint64_t)K, (uint64_t)N_out, (uint64_t)D.N};
-  if (!make_map(&ta, A, 2, da, BM) || !make_map(&tb, B, 3, db, 128)) return cudaErrorInvalidValue;
-  const int64_t max_pairs = (D.R_max / BM + D.N) / 2 * ((N_out + BNP - 1) / BNP);
-  int pairs = num_sms() / 2;
-  if (max_pairs < pairs) pairs = (int)max_pairs;
-  if (pairs < 1) pairs = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * pairs);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemP;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<EPI>, ta, tb, offsets, D.N, D.R_max, (int)K, (int)N_out,
-                            (const __nv_bfloat16 *)bias, row_gate, out, status);
+  return n;
 }
 
 }  // namespace
 
 cudaError_t launch_ffn_tc(const Dims &D, const void *x_perm, const int32_t *offsets, const void *w1, const void *b1,
                           const void *w2, const void *b2, const float *row_gate, void *h, float *y_perm,
-                          int32_t *status, cudaStream_t s) {
-  if (D.dt != MOE_DT_BF16 || D.N > kMaxExperts || D.d > (1 << 30) || D.d_ff > (1 << 30))
+                          int32_t *blk_done, int32_t *status, cudaStream_t s) {
+  if (D.dt != MOE_DT_BF16 || D.N > kMaxExperts || D.d > (1 << 30) || D.d_ff > (1 << 30) || !blk_done)
     return cudaErrorNotSupported;
-  cudaError_t e = launch_pair<1>(D, x_perm, D.d, w1, b1, D.d_ff, nullptr, offsets, h, status, s);
-  if (e != cudaSuccess) return e;
-  return launch_pair<2>(D, h, D.d_ff, w2, b2, D.d, row_gate, offsets, y_perm, status, s);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(ffn_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemP);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  CUtensorMap tx, tw1, th, tw2;
+  const uint64_t dx[2] = {(uint64_t)D.d, (uint64_t)D.R_max};
+  const uint64_t dw1[3] = {(uint64_t)D.d, (uint64_t)D.d_ff, (uint64_t)D.N};
+  const uint64_t dh[2] = {(uint64_t)D.d_ff, (uint64_t)D.R_max};
+  const uint64_t dw2[3] = {(uint64_t)D.d_ff, (uint64_t)D.d, (uint64_t)D.N};
+  if (!make_map(&tx, x_perm, 2, dx, BM) || !make_map(&tw1, w1, 3, dw1, 128) || !make_map(&th, h, 2, dh, BM) ||
+      !make_map(&tw2, w2, 3, dw2, 128))
+    return cudaErrorInvalidValue;
+  const int64_t max_pairs = (int64_t)ffn_blocks_max(D) * (((D.d_ff + BNP - 1) / BNP) + ((D.d + BNP - 1) / BNP));
+  int pairs = resident_pairs();
+  if (max_pairs < pairs) pairs = (int)max_pairs;
+  if (pairs < 1) pairs = 1;
+  return launch_k(ffn_pair_kernel, dim3(2 * pairs), dim3(kThreads), kSmemP, s, 2u, tx, tw1, th, tw2, offsets,
+                  (int)D.N, (int64_t)D.R_max, (int)D.d, (int)D.d_ff, (const __nv_bfloat16 *)b1,
+                  (const __nv_bfloat16 *)b2, row_gate, (__nv_bfloat16 *)h, y_perm, blk_done, (int)ffn_blocks_max(D),
+                  status);
 }
 
 }  // namespace moe

@@ -94,7 +94,7 @@ void make_layout(const Dims &D, moe_workspace_layout *L) {
   L->y_perm = take(R * (size_t)D.d * 4);
   const int S = decode_splits(D);
   L->y_split = take(S > 1 ? (size_t)(S - 1) * R * (size_t)D.d * 4 : 0);
-  L->ffn_sync = take(S > 0 ? N * 4 : 0);
+  L->ffn_sync = take((size_t)ffn_sync_ints(D) * 4);
   L->total = off;
   L->rows = D.R_max;
   L->capacity = D.C;
@@ -138,7 +138,7 @@ moe_status do_dispatch(const Dims &D, const moe_workspace_layout &L, const void 
   int32_t *status = AT(ws, L.status, int32_t *);
   cudaError_t e = launch_capacity(D, topk_idx, gate, score, counts_raw, counts_kept, offsets,
                                   AT(ws, L.sel_thr, uint32_t *), AT(ws, L.sel_eq, int32_t *), row_of, row_token,
-                                  row_gate, status, s);
+                                  row_gate, AT(ws, L.ffn_sync, int32_t *), status, s);
   if (e != cudaSuccess) return cuda_fail(e, "capacity launch");
   e = launch_permute(D, x, offsets, row_token, x_perm, status, s);
   if (e != cudaSuccess) return cuda_fail(e, "permute launch");
@@ -158,7 +158,8 @@ moe_status do_ffn(const Dims &D, const moe_workspace_layout &L, const void *x_pe
     return MOE_OK;
   }
   if (D.dt == MOE_DT_BF16) {
-    cudaError_t e = launch_ffn_tc(D, x_perm, offsets, w1, b1, w2, b2, row_gate, h, y_perm, status, s);
+    cudaError_t e = launch_ffn_tc(D, x_perm, offsets, w1, b1, w2, b2, row_gate, h, y_perm,
+                                  AT(ws, L.ffn_sync, int32_t *), status, s);
     if (e == cudaErrorNotSupported)
       return fail(MOE_ERR_UNSUPPORTED, "expert FFN: shape not supported by the tensor-core kernels");
     if (e != cudaSuccess) return cuda_fail(e, "expert FFN (tensor cores)");
@@ -216,7 +217,11 @@ moe_status moe_workspace_init(const moe_config *cfg, void *ws, moe_stream_t stre
   Dims D;
   TRY(check_config(cfg, &D));
   TRY(check_ptrs({ws}, "moe_workspace_init"));
+  moe_workspace_layout L;
+  make_layout(D, &L);
   cudaError_t e = cudaMemsetAsync(ws, 0, 64, (cudaStream_t)stream);
+  if (e == cudaSuccess && ffn_sync_ints(D) > 0)
+    e = cudaMemsetAsync(AT(ws, L.ffn_sync, void *), 0, (size_t)ffn_sync_ints(D) * 4, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "workspace init");
   return MOE_OK;
 }

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "moe.h"
 
 namespace moe {
@@ -45,6 +47,44 @@ __device__ __forceinline__ void report_error(int32_t *status, int32_t code, int3
     status[1] = kernel;
     status[2] = detail;
   }
+}
+
+// Programmatic dependent launch. Every kernel is launched with programmatic
+// stream serialisation: it may start while the previous kernel of the stream
+// finishes, and waits for that kernel's completion and memory (pdl_wait)
+// before it touches global memory. The persistent tensor-core kernels let
+// their successor launch as soon as a CTA has no work left (pdl_trigger); the
+// other kernels let it launch as their CTAs exit. What overlaps is the launch
+// latency and the prologue (barrier set-up, tensor-memory allocation) that
+// needs no global memory.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch with programmatic stream serialisation (and clusters of `cluster`
+// CTAs along x when cluster > 1).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                            unsigned cluster, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 __device__ __forceinline__ float to_f32(float v) { return v; }
@@ -104,7 +144,7 @@ cudaError_t launch_router_tc(const Dims &D, const void *x, const void *w_g, cons
 cudaError_t launch_capacity(const Dims &D, const int32_t *topk_idx, const float *gate, const float *score,
                             int32_t *counts_raw, int32_t *counts_kept, int32_t *offsets, uint32_t *sel_thr,
                             int32_t *sel_eq, int32_t *row_of, int32_t *row_token, float *row_gate,
-                            int32_t *status, cudaStream_t s);
+                            int32_t *ffn_sync, int32_t *status, cudaStream_t s);
 
 // Number of K slices of the decode-mode second GEMM (>= 1), or 0 when the
 // config is not decode-shaped (bf16 and T*k <= 64*N).
@@ -114,7 +154,8 @@ inline int row_align(const Dims &D) { return decode_splits(D) > 0 ? kDecodeRowsP
 
 // Swap-AB expert FFNs for decode-shaped batches, both GEMMs in one launch.
 // y_split holds the second GEMM's K slices 1..S-1 (S = decode_splits), each
-// [R_max, d] fp32; h_done [N] int32 is reset here and counts stored h tiles.
+// [R_max, d] fp32; h_done [N + 1] int32 counts stored h tiles per expert
+// (zero on entry, left zero on exit).
 cudaError_t launch_ffn_decode(const Dims &D, const void *x_perm, const int32_t *offsets, const void *w1,
                               const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
                               float *y_perm, float *y_split, int32_t *h_done, int32_t *status, cudaStream_t s);
@@ -137,8 +178,25 @@ cudaError_t launch_ffn_simt(const Dims &D, int epi, const void *A, int64_t K, co
 
 // tcgen05 path (bf16). Returns cudaErrorNotSupported when the shape is not
 // handled, so the caller can report MOE_ERR_UNSUPPORTED.
+// Upper bound on the 256-row blocks of the permuted rows (one completion
+// counter each in the fused tensor-core FFN): sum over experts of
+// ceil(segment / 256) <= R_max / 256 + N.
+inline int64_t ffn_blocks_max(const Dims &D) { return D.R_max / 256 + D.N; }
+
+// Completion counters of the fused expert FFNs (bf16 configs): one per
+// expert (decode-shaped) or per 256-row block, plus an exit count. They are
+// zero between launches: set to zero by the workspace init and by every
+// dispatch, and reset by the last CTA of every FFN launch.
+inline int64_t ffn_sync_ints(const Dims &D) {
+  if (D.dt != MOE_DT_BF16) return 0;
+  return (decode_splits(D) > 0 ? (int64_t)D.N : ffn_blocks_max(D)) + 1;
+}
+
+// Both expert GEMMs of a bf16 config in one launch on CTA pairs; blk_done
+// [ffn_blocks_max + 1] int32 counts stored h tiles per block (zero on entry,
+// left zero on exit).
 cudaError_t launch_ffn_tc(const Dims &D, const void *x_perm, const int32_t *offsets, const void *w1,
                           const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
-                          float *y_perm, int32_t *status, cudaStream_t s);
+                          float *y_perm, int32_t *blk_done, int32_t *status, cudaStream_t s);
 
 }  // namespace moe

@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(kWarps * 32) permute_kernel(const uint4 *__res
                                                               const int32_t *__restrict__ row_token, int64_t T,
                                                               int64_t R_max, uint4 *__restrict__ x_perm,
                                                               int32_t *status) {
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int64_t rows = offsets[N];
   if (rows > R_max) rows = R_max;  // a failed assign leaves offsets unchecked; never write past the buffer
@@ -82,6 +83,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float *_
                                                                   const T *__restrict__ x, int64_t T_, int k,
                                                                   int64_t R_max, uint32_t flags,
                                                                   T *__restrict__ y, int32_t *status) {
+  pdl_wait();
   constexpr int U = 8 / KM;
   const int64_t d4 = d >> 2;
   const int64_t items = T_ * d4;
@@ -149,6 +151,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_split_kernel(
     const float *__restrict__ y_perm, const float *__restrict__ y_split, int nsplit, int64_t d,
     const int32_t *__restrict__ row_of, const float *__restrict__ gate, const T *__restrict__ x, int64_t T_, int k,
     int64_t R_max, uint32_t flags, T *__restrict__ y, int32_t *status) {
+  pdl_wait();
   const int64_t d4 = d >> 2;
   const int64_t i = (int64_t)blockIdx.x * kCombineThreads + threadIdx.x;
   if (i >= T_ * d4) return;
@@ -226,9 +229,8 @@ cudaError_t launch_permute(const Dims &D, const void *x, const int32_t *offsets,
                            void *x_perm, int32_t *status, cudaStream_t s) {
   const size_t es = D.dt == MOE_DT_BF16 ? 2 : 4;
   const int64_t vpr = D.d * (int64_t)es / 16;
-  permute_kernel<<<grid_for(D.R_max, kWarps), kWarps * 32, 0, s>>>((const uint4 *)x, vpr, offsets, D.N, row_token,
-                                                                   D.T, D.R_max, (uint4 *)x_perm, status);
-  return cudaGetLastError();
+  return launch_k(permute_kernel, dim3(grid_for(D.R_max, kWarps)), dim3(kWarps * 32), 0, s, 1u, (const uint4 *)x, vpr,
+                  offsets, D.N, row_token, D.T, D.R_max, (uint4 *)x_perm, status);
 }
 
 namespace {
@@ -239,26 +241,16 @@ cudaError_t launch_combine_t(const Dims &D, const float *y_perm, const float *y_
   const int64_t items = D.T * (D.d / 4);
   if (nsplit > 0) {
     const int64_t g = (items + kCombineThreads - 1) / kCombineThreads;
-    combine_split_kernel<T><<<(unsigned)g, kCombineThreads, 0, s>>>(y_perm, y_split, nsplit, D.d, row_of, gate, x,
-                                                                    D.T, D.k, D.R_max, D.flags, y, status);
-    return cudaGetLastError();
+    return launch_k(combine_split_kernel<T>, dim3((unsigned)g), dim3(kCombineThreads), 0, s, 1u, y_perm, y_split,
+                    nsplit, D.d, row_of, gate, x, D.T, D.k, D.R_max, D.flags, y, status);
   }
   const int km = D.k <= 1 ? 1 : D.k <= 2 ? 2 : D.k <= 4 ? 4 : 8;
   const int64_t per_block = (int64_t)kCombineThreads * (8 / km);
   const unsigned g = (unsigned)((items + per_block - 1) / per_block);
-  if (km == 1)
-    combine_kernel<T, 1><<<g, kCombineThreads, 0, s>>>(y_perm, D.d, row_of, gate, x, D.T, D.k, D.R_max, D.flags, y,
-                                                       status);
-  else if (km == 2)
-    combine_kernel<T, 2><<<g, kCombineThreads, 0, s>>>(y_perm, D.d, row_of, gate, x, D.T, D.k, D.R_max, D.flags, y,
-                                                       status);
-  else if (km == 4)
-    combine_kernel<T, 4><<<g, kCombineThreads, 0, s>>>(y_perm, D.d, row_of, gate, x, D.T, D.k, D.R_max, D.flags, y,
-                                                       status);
-  else
-    combine_kernel<T, 8><<<g, kCombineThreads, 0, s>>>(y_perm, D.d, row_of, gate, x, D.T, D.k, D.R_max, D.flags, y,
-                                                       status);
-  return cudaGetLastError();
+  auto kern = km == 1 ? combine_kernel<T, 1> : km == 2 ? combine_kernel<T, 2> : km == 4 ? combine_kernel<T, 4>
+                                                                                    : combine_kernel<T, 8>;
+  return launch_k(kern, dim3(g), dim3(kCombineThreads), 0, s, 1u, y_perm, D.d, row_of, gate, x, D.T, D.k, D.R_max,
+                  D.flags, y, status);
 }
 }  // namespace
 

@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(kWarps * 32) router_small_kernel(const T *__re
                                                                    int d, int N, int k, int32_t *__restrict__ topk_idx,
                                                                    float *__restrict__ gate,
                                                                    float *__restrict__ score) {
+  pdl_wait();
   extern __shared__ uint4 s_w[];  // [N * d * sizeof(T) / 16]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const T *w = w_g;
@@ -284,6 +285,7 @@ __global__ void __launch_bounds__(kWarps * 32) router_kernel(const T *__restrict
                                                              const float *__restrict__ router_bias, int64_t T_,
                                                              int d, int N, int k, int32_t *__restrict__ topk_idx,
                                                              float *__restrict__ gate, float *__restrict__ score) {
+  pdl_wait();
   extern __shared__ float s_logits[];  // [kTokPerBlock][N]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t t0 = ((int64_t)blockIdx.x * kWarps + warp) * kTokPerWarp;
@@ -322,6 +324,7 @@ __global__ void __launch_bounds__(kWarps * 32) router_split_kernel(const T *__re
                                                                    int32_t *__restrict__ topk_idx,
                                                                    float *__restrict__ gate,
                                                                    float *__restrict__ score) {
+  pdl_wait();
   extern __shared__ float s_part[];  // [kWarps][kTokPerWarp][N]
   constexpr int V = VecN<T>::n;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -358,49 +361,41 @@ __global__ void __launch_bounds__(kWarps * 32) router_split_kernel(const T *__re
 
 }  // namespace
 
-cudaError_t launch_router(const Dims &D, const void *x, const void *w_g, const float *router_bias,
-                          int32_t *topk_idx, float *gate, float *score, int32_t *status, cudaStream_t s) {
-  (void)status;
-  const bool bf16 = D.dt == MOE_DT_BF16;
+// The three SIMT router kernels share one argument list.
+template <typename T>
+static cudaError_t launch_router_t(const Dims &D, const T *x, const T *w_g, const float *router_bias,
+                                   int32_t *topk_idx, float *gate, float *score, cudaStream_t s) {
   if (router_split(D)) {
     const unsigned g = (unsigned)((D.T + kTokPerWarp - 1) / kTokPerWarp);
     const size_t smem = sizeof(float) * kWarps * kTokPerWarp * D.N;
-    if (bf16)
-      router_split_kernel<__nv_bfloat16><<<g, kWarps * 32, smem, s>>>(
-          (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)w_g, router_bias, D.T, (int)D.d, D.N, D.k, topk_idx,
-          gate, score);
-    else
-      router_split_kernel<float><<<g, kWarps * 32, smem, s>>>((const float *)x, (const float *)w_g, router_bias,
-                                                              D.T, (int)D.d, D.N, D.k, topk_idx, gate, score);
-    return cudaGetLastError();
+    return launch_k(router_split_kernel<T>, dim3(g), dim3(kWarps * 32), smem, s, 1u, x, w_g, router_bias, D.T,
+                    (int)D.d, D.N, D.k, topk_idx, gate, score);
   }
   const unsigned grid = (unsigned)((D.T + kTokPerBlock - 1) / kTokPerBlock);
   if (D.N <= kEC) {
-    const size_t wbytes = (size_t)D.N * D.d * (bf16 ? 2 : 4);
+    const size_t wbytes = (size_t)D.N * D.d * sizeof(T);
     const bool stage = wbytes <= kMaxStagedW;
     const size_t smem = stage ? wbytes : 0;
-    if (bf16) {
-      auto kern = stage ? router_small_kernel<__nv_bfloat16, true> : router_small_kernel<__nv_bfloat16, false>;
-      if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      kern<<<grid, kWarps * 32, smem, s>>>((const __nv_bfloat16 *)x, (const __nv_bfloat16 *)w_g, router_bias, D.T,
-                                           (int)D.d, D.N, D.k, topk_idx, gate, score);
-    } else {
-      auto kern = stage ? router_small_kernel<float, true> : router_small_kernel<float, false>;
-      if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      kern<<<grid, kWarps * 32, smem, s>>>((const float *)x, (const float *)w_g, router_bias, D.T, (int)D.d, D.N,
-                                           D.k, topk_idx, gate, score);
+    auto kern = stage ? router_small_kernel<T, true> : router_small_kernel<T, false>;
+    if (smem > 48 * 1024) {
+      const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
     }
-  } else {
-    const size_t smem = sizeof(float) * kTokPerBlock * D.N;
-    if (bf16)
-      router_kernel<__nv_bfloat16><<<grid, kWarps * 32, smem, s>>>((const __nv_bfloat16 *)x,
-                                                                   (const __nv_bfloat16 *)w_g, router_bias, D.T,
-                                                                   (int)D.d, D.N, D.k, topk_idx, gate, score);
-    else
-      router_kernel<float><<<grid, kWarps * 32, smem, s>>>((const float *)x, (const float *)w_g, router_bias, D.T,
-                                                           (int)D.d, D.N, D.k, topk_idx, gate, score);
+    return launch_k(kern, dim3(grid), dim3(kWarps * 32), smem, s, 1u, x, w_g, router_bias, D.T, (int)D.d, D.N, D.k,
+                    topk_idx, gate, score);
   }
-  return cudaGetLastError();
+  const size_t smem = sizeof(float) * kTokPerBlock * D.N;
+  return launch_k(router_kernel<T>, dim3(grid), dim3(kWarps * 32), smem, s, 1u, x, w_g, router_bias, D.T, (int)D.d,
+                  D.N, D.k, topk_idx, gate, score);
+}
+
+cudaError_t launch_router(const Dims &D, const void *x, const void *w_g, const float *router_bias,
+                          int32_t *topk_idx, float *gate, float *score, int32_t *status, cudaStream_t s) {
+  (void)status;
+  if (D.dt == MOE_DT_BF16)
+    return launch_router_t(D, (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)w_g, router_bias, topk_idx, gate,
+                           score, s);
+  return launch_router_t(D, (const float *)x, (const float *)w_g, router_bias, topk_idx, gate, score, s);
 }
 
 }  // namespace moe

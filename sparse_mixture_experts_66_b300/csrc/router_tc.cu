@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = c->tmem_base;
+  pdl_wait();  // x and W_g may come from the previous kernel; the outputs may still be read by it
 
   if (warp == 0) {
     if (lane == 0) {
@@ -226,6 +227,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
     }
   }
 
+  pdl_trigger();  // the next kernel may launch while this one tears down
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -250,9 +252,8 @@ cudaError_t launch_np(const Dims &D, const void *x, const void *w_g, const float
   const uint64_t dw[2] = {(uint64_t)D.d, (uint64_t)D.N};
   if (!make_map(&tx, x, 2, dx, kRM) || !make_map(&tw, w_g, 2, dw, NP)) return cudaErrorInvalidValue;
   const unsigned grid = (unsigned)((D.T + kRM - 1) / kRM);
-  router_tc_kernel<NP><<<grid, kRThreads, smem, s>>>(tx, tw, router_bias, D.T, (int)D.d, D.N, D.k, topk_idx, gate,
-                                                     score, status);
-  return cudaGetLastError();
+  return launch_k(router_tc_kernel<NP>, dim3(grid), dim3(kRThreads), smem, s, 1u, tx, tw, router_bias, D.T, (int)D.d,
+                  D.N, D.k, topk_idx, gate, score, status);
 }
 
 }  // namespace

@@ -63,6 +63,37 @@ static __device__ __noinline__ bool mbar_wait(unsigned long long *bar, uint32_t 
 }
 
 
+// Cross-CTA hand-off of data written with ordinary stores and read by TMA:
+// the writer fences its stores for the async proxy and then releases a
+// counter; the reader acquires the counter and fences before its TMA loads.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ void red_release_add(int32_t *p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire(const int32_t *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Bounded wait until *p >= need (acquire). False on timeout (MOE_ERR_TIMEOUT
+// recorded, abort raised) or when another role has aborted.
+static __device__ __noinline__ bool wait_counter(const int32_t *p, int need, volatile int *abort, int32_t *status,
+                                          int kernel, int where) {
+  if (ld_acquire(p) >= need) return true;
+  const unsigned long long t0 = globaltimer();
+  while (ld_acquire(p) < need) {
+    if (*abort) return false;
+    if (globaltimer() - t0 > kTimeoutNs) {
+      report_error(status, MOE_ERR_TIMEOUT, kernel, where);
+      *abort = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
