@@ -312,9 +312,12 @@ __global__ void __launch_bounds__(kDThreads, 1)
         if (tl.phase == 0) {
           if (fvalid) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < 32; j += 2) {
               const int64_t row = (int64_t)tl.row0 + c0 + j;
-              h[row * d_ff + f] = __float2bfloat16_rn(gelu_as(__uint_as_float(r[j]) + b));
+              const float2 a = gelu_as2(__fadd2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                                                   make_float2(b, b)));
+              h[row * d_ff + f] = __float2bfloat16_rn(a.x);
+              h[(row + 1) * d_ff + f] = __float2bfloat16_rn(a.y);
             }
           }
         } else {

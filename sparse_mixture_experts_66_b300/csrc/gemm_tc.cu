@@ -402,24 +402,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool store = valid && n + g8 * 8 < N_out;
           const uint4 braw = sbias[cc * 4 + g8];
           const uint32_t bw[4] = {braw.x, braw.y, braw.z, braw.w};
-          float v[8];
+          float2 v[4];  // accumulator + bias, column pairs
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            v[2 * j] = __uint_as_float(r[g8 * 8 + 2 * j]) + __uint_as_float(bw[j] << 16);
-            v[2 * j + 1] = __uint_as_float(r[g8 * 8 + 2 * j + 1]) + __uint_as_float(bw[j] & 0xffff0000u);
-          }
+          for (int j = 0; j < 4; ++j)
+            v[j] = __fadd2_rn(make_float2(__uint_as_float(r[g8 * 8 + 2 * j]), __uint_as_float(r[g8 * 8 + 2 * j + 1])),
+                              make_float2(__uint_as_float(bw[j] << 16), __uint_as_float(bw[j] & 0xffff0000u)));
           if (tl.phase == 0) {
             uint32_t pk[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              __nv_bfloat162 h2 = __floats2bfloat162_rn(gelu_as(v[2 * j]), gelu_as(v[2 * j + 1]));
+              const float2 a = gelu_as2(v[j]);
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(a.x, a.y);
               pk[j] = *reinterpret_cast<uint32_t *>(&h2);
             }
             if (store) *reinterpret_cast<uint4 *>(h + row * d_ff + n + g8 * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           } else if (store) {
+            const float2 g2 = make_float2(g, g);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = __fmul2_rn(v[j], g2);
             float *o = y_perm + row * d + n + g8 * 8;
-            *reinterpret_cast<float4 *>(o) = make_float4(g * v[0], g * v[1], g * v[2], g * v[3]);
-            *reinterpret_cast<float4 *>(o + 4) = make_float4(g * v[4], g * v[5], g * v[6], g * v[7]);
+            *reinterpret_cast<float4 *>(o) = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
+            *reinterpret_cast<float4 *>(o + 4) = make_float4(v[2].x, v[2].y, v[3].x, v[3].y);
           }
         }
       }
