@@ -135,10 +135,15 @@ __device__ __forceinline__ void umma_commit_pair(unsigned long long *bar, uint16
 // to the block's counter; the GEMM2 producers acquire it before loading h.
 // The order is deadlock-free with all pairs resident: a tile only waits on
 // tiles earlier in the list, and each pair walks its tiles in list order.
+// (Handing tiles out through a global counter instead measured slower here:
+// per-tile data waits grew more than the balance improved.)
 //
-// Tiles: per expert, pair tiles of 256 rows (two 128-row segment tiles); when
-// an expert has an odd number of 128-row tiles, the peer's half of its last
-// pair tile lies past the segment and its rows are computed but not stored.
+// Tiles: per expert, pair tiles of 256 rows (two 128-row segment tiles). When
+// an expert has an odd number of 128-row tiles, its last pair tile is a
+// 128-row tail computed with the operands swapped: the 256 weight rows on M
+// (128 per CTA, loaded exactly like the B half of a normal tile) and the 128
+// tail rows on N (64 per CTA), tcgen05.mma M=256, N=128, so no padding rows
+// are computed; its epilogue stores one feature per thread across the tokens.
 constexpr int kStagesP = 6;
 constexpr int kAP = BM * BK * 2;          // 16 KB: this CTA's 128 rows of A
 constexpr int kBP = 128 * BK * 2;         // 16 KB: this CTA's half of the B tile
@@ -152,6 +157,7 @@ struct PTile {
   int m0;     // first row of the 256-row pair tile
   int ni;     // n-tile
   int blk;    // index of the 256-row block (dependency counter)
+  int swap;   // a 128-row tail, computed with the operands swapped
 };
 
 __device__ __forceinline__ PTile decode_pair_tile(const Ctrl *c, int N_exp, int t) {
@@ -171,6 +177,7 @@ __device__ __forceinline__ PTile decode_pair_tile(const Ctrl *c, int N_exp, int 
   const int pb = local - p.ni * mp;
   p.m0 = c->offsets[lo] + pb * (2 * BM);
   p.blk = c->blk_start[lo] + pb;
+  p.swap = pb == mp - 1 && (((c->offsets[lo + 1] - c->offsets[lo]) / BM) & 1);
   return p;
 }
 
@@ -190,10 +197,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
-  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const int n1 = (d_ff + BNP - 1) / BNP, n2 = (d + BNP - 1) / BNP;
   const int kb1 = (d + BK - 1) / BK, kb2 = (d_ff + BK - 1) / BK;
   const int need = n1 * 2 * kEpiWarps;  // epilogue-warp arrivals that complete a 256-row block of h
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
   if (warp == 0) {
     pdl_wait();  // offsets come from the dispatch
@@ -278,7 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t full_leader0 = map_to_rank(saddr(&c->full[0]), 0);
       for (int t = pair; ok && t < total; t += npairs) {
         const PTile tl = decode_pair_tile(c, N_exp, t);
-        const int a_row = tl.m0 + (int)rank * BM, b_row = tl.ni * BNP + (int)rank * 128;
+        // tokens: this CTA's 128 rows, or for a swapped tail its 64 (of a 128-row box)
+        const int a_row = tl.m0 + (int)rank * (tl.swap ? BM / 2 : BM), b_row = tl.ni * BNP + (int)rank * 128;
         const CUtensorMap *ma = tl.phase ? &tm_h : &tm_x;
         const CUtensorMap *mb = tl.phase ? &tm_w2 : &tm_w1;
         const int kbn = tl.phase ? kb2 : kb1;
@@ -320,12 +328,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true, any = false;
       const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BNP >> 3) << 17) |
                              ((uint32_t)((2 * BM) >> 4) << 24);
+      // swapped tail: weights on M (256 features), the 128 tail tokens on N
+      const uint32_t idesc_swap = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BM >> 3) << 17) |
+                                  ((uint32_t)((2 * BM) >> 4) << 24);
       // stage buffers are equally spaced: a stage's descriptor is the first one
       // advanced by the stage offset in 16-byte units (no carry out of the
       // 14-bit address field below 256 KB)
       const uint64_t adesc0 = smem_desc_sw128(saddr(sA)), bdesc0 = smem_desc_sw128(saddr(sB));
       for (int t = pair; ok && t < total; t += npairs) {
-        const int kbn = t >= c->total1 ? kb2 : kb1;
+        const PTile tl = decode_pair_tile(c, N_exp, t);
+        const int kbn = tl.phase ? kb2 : kb1;
+        const uint32_t id = tl.swap ? idesc_swap : idesc;
+        const uint64_t da0 = tl.swap ? bdesc0 : adesc0, db0 = tl.swap ? adesc0 : bdesc0;
         if (!mbar_wait_fast(&c->tempty[acc], aph ^ 1u, abort, status, kKGemmTc, 60 + acc)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + (uint32_t)(acc * BNP);
@@ -335,10 +349,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t ad = adesc0 + (uint64_t)(s * (kAP >> 4)), bd = bdesc0 + (uint64_t)(s * (kBP >> 4));
+          static_assert(kAP == kBP, "A and B stage buffers advance by the same stride");
+          const uint64_t ad = da0 + (uint64_t)(s * (kAP >> 4)), bd = db0 + (uint64_t)(s * (kBP >> 4));
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
-            umma_bf16_pair(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, (kb | kk) != 0 ? 1u : 0u);
+            umma_bf16_pair(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), id, (kb | kk) != 0 ? 1u : 0u);
           any = true;
           umma_commit_pair(&c->empty[s], (uint16_t)0x3);
           if (++s == kStagesP) {
@@ -362,6 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int part = (warp - 2) >> 2;  // which share of the tile's columns (warps per lane quarter split them)
     constexpr int kCols = BNP / (kEpiWarps / 4);
+    constexpr int kSwapCols = BM / (kEpiWarps / 4);  // token columns per warp of a swapped tail
+    static_assert(kSwapCols == 32 || kSwapCols == 64, "swapped-tail column split");
     const int row_in_tile = (int)rank * BM + q * 32 + lane;
     const uint32_t tempty_leader0 = map_to_rank(saddr(&c->tempty[0]), 0);
     const uint32_t tempty_leader1 = map_to_rank(saddr(&c->tempty[1]), 0);
@@ -372,57 +389,100 @@ __global__ void __launch_bounds__(kThreads, 1)
       const PTile tl = decode_pair_tile(c, N_exp, t);
       // everything the tile's epilogue reads from memory is fetched before the
       // accumulator wait, so no load latency sits between TMEM and the stores
+      const int N_out = tl.phase ? d : d_ff;
+      const __nv_bfloat16 *bias = tl.phase ? b2 : b1;
+      // normal tile: this thread's row, its gate, the warp's bias columns
       const int64_t row = (int64_t)tl.m0 + row_in_tile;
       const bool valid = row < c->offsets[tl.e + 1];
-      const int N_out = tl.phase ? d : d_ff;
-      const float g = (tl.phase && row_gate && valid) ? row_gate[row] : 1.0f;
-      {
-        const __nv_bfloat16 *bias = tl.phase ? b2 : b1;
+      float g = 1.0f;
+      // swapped tail: this thread's feature, its bias, the gates of the warp's token columns
+      const int f = tl.ni * BNP + (int)rank * 128 + q * 32 + lane;
+      float bsw = 0.f, glo = 1.f, ghi = 1.f;
+      if (!tl.swap) {
+        if (tl.phase && row_gate && valid) g = row_gate[row];
         const int nb = tl.ni * BNP + part * kCols + lane * 8;
         __syncwarp();  // the previous tile's reads of sbias are done
         if (lane < kCols / 8)
           sbias[lane] = nb < N_out ? __ldg(reinterpret_cast<const uint4 *>(bias + (int64_t)tl.e * N_out + nb))
                                    : make_uint4(0u, 0u, 0u, 0u);
         __syncwarp();
+      } else {
+        if (f < N_out) bsw = __bfloat162float(bias[(int64_t)tl.e * N_out + f]);
+        if (tl.phase && row_gate) {
+          glo = row_gate[tl.m0 + part * kSwapCols + lane];
+          if (kSwapCols > 32) ghi = row_gate[tl.m0 + part * kSwapCols + 32 + lane];
+        }
       }
       int ok = 0;
       if (lane == 0) ok = mbar_wait(&c->tfull[acc], aph, abort, status, kKGemmTc, 80 + acc) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
+      if (tl.swap) {
+        // D^T: TMEM lane = feature f, column = token row m0 + column; the tail's
+        // 128 rows all lie inside the expert's segment
+        const bool fvalid = f < N_out;
 #pragma unroll 1
-      for (int cc = 0; cc < kCols / 32; ++cc) {
-        const int col0 = part * kCols + cc * 32;
-        uint32_t r[32];
-        __syncwarp();  // the TMEM load is warp-collective: reconverge after the row-masked stores
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BNP + col0), r);
-        const int n = tl.ni * BNP + col0;
-#pragma unroll
-        for (int g8 = 0; g8 < 4; ++g8) {
-          const bool store = valid && n + g8 * 8 < N_out;
-          const uint4 braw = sbias[cc * 4 + g8];
-          const uint32_t bw[4] = {braw.x, braw.y, braw.z, braw.w};
-          float2 v[4];  // accumulator + bias, column pairs
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            v[j] = __fadd2_rn(make_float2(__uint_as_float(r[g8 * 8 + 2 * j]), __uint_as_float(r[g8 * 8 + 2 * j + 1])),
-                              make_float2(__uint_as_float(bw[j] << 16), __uint_as_float(bw[j] & 0xffff0000u)));
+        for (int cc = 0; cc < kSwapCols / 32; ++cc) {
+          const int c0 = part * kSwapCols + cc * 32;
+          uint32_t r[32];
+          __syncwarp();
+          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BNP + c0), r);
           if (tl.phase == 0) {
-            uint32_t pk[4];
+            if (fvalid) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float2 a = gelu_as2(v[j]);
-              __nv_bfloat162 h2 = __floats2bfloat162_rn(a.x, a.y);
-              pk[j] = *reinterpret_cast<uint32_t *>(&h2);
+              for (int j = 0; j < 32; j += 2) {
+                const float2 a = gelu_as2(
+                    __fadd2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), make_float2(bsw, bsw)));
+                const int64_t rr = (int64_t)tl.m0 + c0 + j;
+                h[rr * d_ff + f] = __float2bfloat16_rn(a.x);
+                h[(rr + 1) * d_ff + f] = __float2bfloat16_rn(a.y);
+              }
             }
-            if (store) *reinterpret_cast<uint4 *>(h + row * d_ff + n + g8 * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          } else if (store) {
-            const float2 g2 = make_float2(g, g);
+          } else {
+            const float gsrc = cc == 0 ? glo : ghi;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = __fmul2_rn(v[j], g2);
-            float *o = y_perm + row * d + n + g8 * 8;
-            *reinterpret_cast<float4 *>(o) = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
-            *reinterpret_cast<float4 *>(o + 4) = make_float4(v[2].x, v[2].y, v[3].x, v[3].y);
+            for (int j = 0; j < 32; ++j) {
+              const float gj = __shfl_sync(0xffffffffu, gsrc, j);
+              if (fvalid) y_perm[((int64_t)tl.m0 + c0 + j) * d + f] = gj * (__uint_as_float(r[j]) + bsw);
+            }
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int cc = 0; cc < kCols / 32; ++cc) {
+          const int col0 = part * kCols + cc * 32;
+          uint32_t r[32];
+          __syncwarp();  // the TMEM load is warp-collective: reconverge after the row-masked stores
+          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BNP + col0), r);
+          const int n = tl.ni * BNP + col0;
+#pragma unroll
+          for (int g8 = 0; g8 < 4; ++g8) {
+            const bool store = valid && n + g8 * 8 < N_out;
+            const uint4 braw = sbias[cc * 4 + g8];
+            const uint32_t bw[4] = {braw.x, braw.y, braw.z, braw.w};
+            float2 v[4];  // accumulator + bias, column pairs
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              v[j] = __fadd2_rn(make_float2(__uint_as_float(r[g8 * 8 + 2 * j]), __uint_as_float(r[g8 * 8 + 2 * j + 1])),
+                                make_float2(__uint_as_float(bw[j] << 16), __uint_as_float(bw[j] & 0xffff0000u)));
+            if (tl.phase == 0) {
+              uint32_t pk[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const float2 a = gelu_as2(v[j]);
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(a.x, a.y);
+                pk[j] = *reinterpret_cast<uint32_t *>(&h2);
+              }
+              if (store) *reinterpret_cast<uint4 *>(h + row * d_ff + n + g8 * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            } else if (store) {
+              const float2 g2 = make_float2(g, g);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) v[j] = __fmul2_rn(v[j], g2);
+              float *o = y_perm + row * d + n + g8 * 8;
+              *reinterpret_cast<float4 *>(o) = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
+              *reinterpret_cast<float4 *>(o + 4) = make_float4(v[2].x, v[2].y, v[3].x, v[3].y);
+            }
           }
         }
       }
@@ -453,8 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __threadfence();
     if (atomicAdd(blk_done + nblk_max, 1) == (int)gridDim.x - 1) {
       __threadfence();
-      for (int i = 0; i < nblk_max; ++i) blk_done[i] = 0;
-      blk_done[nblk_max] = 0;
+      for (int i = 0; i <= nblk_max; ++i) blk_done[i] = 0;
     }
   }
 }

@@ -33,12 +33,14 @@ template <int NP> struct RCfg {
   static constexpr int kXBytes = kRM * kRBK * 2;
   static constexpr int kWBytes = NP * kRBK * 2;
   static constexpr int kStageBytes = kXBytes + kWBytes;
-  static constexpr int kStages = (96 * 1024) / kStageBytes < 2 ? 2 : ((96 * 1024) / kStageBytes > 6 ? 6 : (96 * 1024) / kStageBytes);
+  // as many stages as fit 192 KB (2..12): few CTAs stream all of x, so each
+  // needs many bytes in flight
+  static constexpr int kStages = (192 * 1024) / kStageBytes < 2 ? 2 : ((192 * 1024) / kStageBytes > 12 ? 12 : (192 * 1024) / kStageBytes);
   static constexpr int kTmemCols = NP < 32 ? 32 : NP;  // a power of two >= 32
 };
 
 struct RCtrl {
-  unsigned long long full[8], empty[8], tfull, drain;
+  unsigned long long full[12], empty[12], tfull, drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -90,8 +92,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
     if (lane == 0) {
       int s = 0;
       uint32_t ph = 0;
-      bool issued[8] = {false, false, false, false, false, false, false, false};
-      uint32_t issued_parity[8];
+      uint32_t issued_mask = 0, parity_mask = 0;  // stages with a copy issued, and its phase parity
       bool ok = true;
       for (int kb = 0; kb < kb_count; ++kb) {
         if (!mbar_wait_fast(&c->empty[s], ph ^ 1u, abort, status, kKRouter, 10 + s)) {
@@ -101,8 +102,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
         mbar_expect_tx(&c->full[s], C::kStageBytes);
         tma_load_2d(sX + s * C::kXBytes, &tm_x, &c->full[s], kb * kRBK, (int)t0);
         tma_load_2d(sW + s * C::kWBytes, &tm_w, &c->full[s], kb * kRBK, 0);
-        issued[s] = true;
-        issued_parity[s] = ph;
+        issued_mask |= 1u << s;
+        parity_mask = (parity_mask & ~(1u << s)) | (ph << s);
         if (++s == C::kStages) {
           s = 0;
           ph ^= 1u;
@@ -110,9 +111,9 @@ __global__ void __launch_bounds__(kRThreads, 1)
       }
       if (!ok) {
         for (int i = 0; i < C::kStages; ++i)
-          if (issued[i]) {
+          if (issued_mask & (1u << i)) {
             const unsigned long long ts = globaltimer();
-            while (!mbar_try_wait(&c->full[i], issued_parity[i]) && globaltimer() - ts < kTimeoutNs) {
+            while (!mbar_try_wait(&c->full[i], (parity_mask >> i) & 1u) && globaltimer() - ts < kTimeoutNs) {
             }
           }
       }
