@@ -302,7 +302,6 @@ def run_ours(args, world, rank, local):
         ev_f[i][1].record(stream)
         st.combine(stream)
     torch.cuda.synchronize(device)
-    clk = clocks.stop()
     ws.status(stream)
     ffn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_f)
 
@@ -323,6 +322,7 @@ def run_ours(args, world, rank, local):
     stage_ms = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev2)
                 for j, n in enumerate(["route", "dispatch", "expert_ffn", "combine"])}
     stage_ms["serialised_step"] = statistics.mean(e[0].elapsed_time(e[4]) for e in ev2)
+    clk = clocks.stop()
     value, slowest_s = aggregate_throughput(w.T, ms * 1e-3, world, device)
     ms_max = slowest_s * 1e3
 

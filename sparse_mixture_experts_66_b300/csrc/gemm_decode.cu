@@ -39,10 +39,14 @@ using namespace tc;
 
 constexpr int kDM = 128;  // weight rows per tile (MMA M)
 constexpr int kDN = 64;   // token rows per chunk (MMA N)
-constexpr int kDBK = 64;  // k-block
-constexpr int kDStages = 8;
-constexpr int kDWBytes = kDM * kDBK * 2;
-constexpr int kDTBytes = kDN * kDBK * 2;
+constexpr int kDAtom = 64;                // columns of one 128-byte swizzle atom (one TMA box)
+constexpr int kDAtoms = 2;                // atoms per stage: each weight row is requested 256 B at a time
+constexpr int kDBK = kDAtom * kDAtoms;    // k-block
+constexpr int kDStages = 8 / kDAtoms;
+constexpr int kDWAtomBytes = kDM * kDAtom * 2;
+constexpr int kDTAtomBytes = kDN * kDAtom * 2;
+constexpr int kDWBytes = kDWAtomBytes * kDAtoms;
+constexpr int kDTBytes = kDTAtomBytes * kDAtoms;
 constexpr int kDStageBytes = kDWBytes + kDTBytes;
 constexpr int kDThreads = 192;
 constexpr int kDMaxExperts = 256;
@@ -206,13 +210,15 @@ __global__ void __launch_bounds__(kDThreads, 1)
             break;
           }
           mbar_expect_tx(&c->full[s], kDStageBytes);
-          if (tl.phase == 0) {
-            tma_load_3d(sW + s * kDWBytes, &tm_w1, &c->full[s], kb * kDBK, tl.m * kDM, tl.e);
-            tma_load_2d(sT + s * kDTBytes, &tm_x, &c->full[s], kb * kDBK, tl.row0);
-          } else {
-            tma_load_3d(sW + s * kDWBytes, &tm_w2, &c->full[s], kb * kDBK, tl.m * kDM, tl.e);
-            tma_load_2d(sT + s * kDTBytes, &tm_h, &c->full[s], kb * kDBK, tl.row0);
-          }
+          const CUtensorMap *mw = tl.phase ? &tm_w2 : &tm_w1;
+          const CUtensorMap *mt = tl.phase ? &tm_h : &tm_x;
+#pragma unroll
+          for (int a = 0; a < kDAtoms; ++a)  // columns past K are zero-filled by TMA
+            tma_load_3d(sW + s * kDWBytes + a * kDWAtomBytes, mw, &c->full[s], kb * kDBK + a * kDAtom, tl.m * kDM,
+                        tl.e);
+#pragma unroll
+          for (int a = 0; a < kDAtoms; ++a)
+            tma_load_2d(sT + s * kDTBytes + a * kDTAtomBytes, mt, &c->full[s], kb * kDBK + a * kDAtom, tl.row0);
           issued_mask |= 1u << s;
           parity_mask = (parity_mask & ~(1u << s)) | (ph << s);
           if (++s == kDStages) {
@@ -257,8 +263,10 @@ __global__ void __launch_bounds__(kDThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kDBK / 16; ++kk)
-            umma_bf16_cta1(d_tmem, wdesc0 + (uint64_t)(s * (kDWBytes >> 4) + 2 * kk),
-                           tdesc0 + (uint64_t)(s * (kDTBytes >> 4) + 2 * kk), idesc,
+            umma_bf16_cta1(d_tmem,
+                           wdesc0 + (uint64_t)(s * (kDWBytes >> 4) + (kk >> 2) * (kDWAtomBytes >> 4) + 2 * (kk & 3)),
+                           tdesc0 + (uint64_t)(s * (kDTBytes >> 4) + (kk >> 2) * (kDTAtomBytes >> 4) + 2 * (kk & 3)),
+                           idesc,
                            (kb != kb0 || kk != 0) ? 1u : 0u);
           any = true;
           umma_commit_cta1(&c->empty[s]);
