@@ -71,11 +71,12 @@ template <> struct Store4<__nv_bfloat16> {
   }
 };
 
-// Combine, without K slices: each thread owns 4 columns of U tokens
-// (U = 8 / KM, KM >= k), so a thread first has U x KM row indices and then
-// U x KM 16-byte rows in flight at once; the loads are unconditional (a
-// dropped pick reads row 0 and is masked out), so nothing serialises them.
-// The picks of a token are added in pick order.
+// Combine, without K slices: a CTA owns U = 8 / KM tokens (KM >= k) and its
+// threads stride over their columns 4 at a time. A thread reads the U x KM
+// row indices once, then keeps U x KM 16-byte row loads in flight per column
+// group; the loads are unconditional (a dropped pick reads row 0 and is masked
+// out), so nothing serialises them, and no index division is needed. The
+// picks of a token are added in pick order.
 template <typename T, int KM>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float *__restrict__ y_perm, int64_t d,
                                                                   const int32_t *__restrict__ row_of,
@@ -85,60 +86,62 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float *_
                                                                   T *__restrict__ y, int32_t *status) {
   pdl_wait();
   constexpr int U = 8 / KM;
-  const int64_t d4 = d >> 2;
-  const int64_t items = T_ * d4;
-  int64_t tok[U], col[U];
-  int32_t rows[U][KM];
+  const int64_t t0 = (int64_t)blockIdx.x * U;
+  int64_t rows[U][KM];  // row of each pick, or -1 (dropped / out of range)
+  float ksum[U];        // kept-gate sum (for MOE_FLAG_RENORM_SURVIVORS)
+  bool renorm[U];       // divide by ksum
+  bool ident[U];        // identity fallback: every pick dropped
 #pragma unroll
   for (int u = 0; u < U; ++u) {
-    const int64_t i = ((int64_t)blockIdx.x * U + u) * kCombineThreads + threadIdx.x;
-    tok[u] = i < items ? i / d4 : -1;
-    col[u] = i < items ? (i - tok[u] * d4) << 2 : 0;
-#pragma unroll
-    for (int j = 0; j < KM; ++j) rows[u][j] = (tok[u] >= 0 && j < k) ? __ldg(row_of + tok[u] * k + j) : -1;
-  }
-  float4 acc[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    float4 v[KM];
-#pragma unroll
-    for (int j = 0; j < KM; ++j) {
-      const int64_t r = (rows[u][j] >= 0 && rows[u][j] < R_max) ? rows[u][j] : 0;
-      v[j] = __ldg(reinterpret_cast<const float4 *>(y_perm + r * d + col[u]));
-    }
-    acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int j = 0; j < KM; ++j) {
-      if (rows[u][j] >= 0 && rows[u][j] < R_max) {
-        acc[u].x += v[j].x;
-        acc[u].y += v[j].y;
-        acc[u].z += v[j].z;
-        acc[u].w += v[j].w;
-      }
-    }
-  }
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    if (tok[u] < 0) continue;
+    const int64_t t = t0 + u;
     int nkept = 0;
     float kept_gate = 0.f;
 #pragma unroll
     for (int j = 0; j < KM; ++j) {
-      if (rows[u][j] >= R_max && col[u] == 0) report_error(status, MOE_ERR_BOUNDS, kKCombine, (int32_t)tok[u]);
-      if (rows[u][j] >= 0 && rows[u][j] < R_max) {
+      int32_t r = (t < T_ && j < k) ? __ldg(row_of + t * k + j) : -1;
+      if (r >= R_max) {
+        if (threadIdx.x == 0) report_error(status, MOE_ERR_BOUNDS, kKCombine, (int32_t)t);
+        r = -1;
+      }
+      rows[u][j] = r;
+      if (r >= 0) {
         ++nkept;
-        if (flags & MOE_FLAG_RENORM_SURVIVORS) kept_gate += __ldg(gate + tok[u] * k + j);
+        if (flags & MOE_FLAG_RENORM_SURVIVORS) kept_gate += __ldg(gate + t * k + j);
       }
     }
-    float4 a = acc[u];
-    if ((flags & MOE_FLAG_RENORM_SURVIVORS) && nkept > 0) {
-      a.x /= kept_gate;
-      a.y /= kept_gate;
-      a.z /= kept_gate;
-      a.w /= kept_gate;
+    ksum[u] = kept_gate;
+    renorm[u] = (flags & MOE_FLAG_RENORM_SURVIVORS) && nkept > 0;
+    ident[u] = (flags & MOE_FLAG_IDENTITY_FALLBACK) && nkept == 0;
+  }
+  for (int64_t c = (int64_t)threadIdx.x * 4; c < d; c += kCombineThreads * 4) {
+    float4 v[U][KM];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int j = 0; j < KM; ++j)
+        v[u][j] = __ldg(reinterpret_cast<const float4 *>(y_perm + (rows[u][j] >= 0 ? rows[u][j] : 0) * d + c));
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (t0 + u >= T_) continue;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < KM; ++j) {
+        if (rows[u][j] >= 0) {
+          a.x += v[u][j].x;
+          a.y += v[u][j].y;
+          a.z += v[u][j].z;
+          a.w += v[u][j].w;
+        }
+      }
+      if (renorm[u]) {
+        a.x /= ksum[u];
+        a.y /= ksum[u];
+        a.z /= ksum[u];
+        a.w /= ksum[u];
+      }
+      if (ident[u]) a = Store4<T>::ld(x + (t0 + u) * d + c);
+      Store4<T>::st(y + (t0 + u) * d + c, a);
     }
-    if ((flags & MOE_FLAG_IDENTITY_FALLBACK) && nkept == 0) a = Store4<T>::ld(x + tok[u] * d + col[u]);
-    Store4<T>::st(y + tok[u] * d + col[u], a);
   }
 }
 
@@ -245,8 +248,8 @@ cudaError_t launch_combine_t(const Dims &D, const float *y_perm, const float *y_
                     nsplit, D.d, row_of, gate, x, D.T, D.k, D.R_max, D.flags, y, status);
   }
   const int km = D.k <= 1 ? 1 : D.k <= 2 ? 2 : D.k <= 4 ? 4 : 8;
-  const int64_t per_block = (int64_t)kCombineThreads * (8 / km);
-  const unsigned g = (unsigned)((items + per_block - 1) / per_block);
+  const int64_t tok_per_block = 8 / km;
+  const unsigned g = (unsigned)((D.T + tok_per_block - 1) / tok_per_block);
   auto kern = km == 1 ? combine_kernel<T, 1> : km == 2 ? combine_kernel<T, 2> : km == 4 ? combine_kernel<T, 4>
                                                                                     : combine_kernel<T, 8>;
   return launch_k(kern, dim3(g), dim3(kCombineThreads), 0, s, 1u, y_perm, D.d, row_of, gate, x, D.T, D.k, D.R_max,

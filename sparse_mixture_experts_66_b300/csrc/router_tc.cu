@@ -43,6 +43,7 @@ struct RCtrl {
   unsigned long long full[12], empty[12], tfull, drain;
   uint32_t tmem_base;
   int abort;
+  float bias[256];  // the logit bias (0 when none), for every padded expert column
 };
 
 template <int NP> constexpr size_t router_smem() {
@@ -155,6 +156,10 @@ __global__ void __launch_bounds__(kRThreads, 1)
   } else {
     const int q = warp & 3;
     const int64_t t = t0 + q * 32 + lane;
+    // the epilogue warps stage the logit bias (0 when none) while the MMAs run
+    for (int i = threadIdx.x - 64; i < NP; i += kRThreads - 64)
+      c->bias[i] = (router_bias && i < N) ? router_bias[i] : 0.f;
+    asm volatile("bar.sync 1, %0;" ::"n"(kRThreads - 64) : "memory");  // the 4 epilogue warps only
     int ok = 0;
     if (lane == 0) ok = mbar_wait(&c->tfull, 0, abort, status, kKRouter, 30) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -177,9 +182,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           int e = c0 + j;
-          if (e >= N) break;
-          float v = __uint_as_float(r[j]);
-          if (router_bias) v += router_bias[e];
+          if (e >= N) break;  // padded expert columns
+          float v = __uint_as_float(r[j]) + c->bias[e];
           m = fmaxf(m, v);
 #pragma unroll
           for (int s = 0; s < 8; ++s) {
@@ -204,9 +208,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
         for (int j = 0; j < 32; ++j) {
           const int e = c0 + j;
           if (e >= N) break;
-          float v = __uint_as_float(r[j]);
-          if (router_bias) v += router_bias[e];
-          sum += expf(v - m);
+          sum += expf(__uint_as_float(r[j]) + c->bias[e] - m);
         }
       }
       if (t < T_) {

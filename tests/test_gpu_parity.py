@@ -34,6 +34,10 @@ STAGE_CASES = [
     custom(512, 64, 64, 256, 8, 1.0, seed=4),
     # every fp32 score of expert 0 rounds to 1.0: a full tie, resolved by token order
     custom(400, 128, 256, 8, 2, 1.0, router_bias="const:0:30", seed=9),
+    # more requests than one pass of the capacity CTA holds: compacted per expert, with overflow
+    custom(6000, 64, 64, 8, 2, 1.0, router_bias="zipf", seed=17),
+    # expert 0 receives more requests than the compacted list holds (16384): the multi-pass fallback
+    custom(20000, 64, 64, 4, 2, 1.0, router_bias="const:0:6", seed=18),
 ]
 
 
