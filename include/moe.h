@@ -76,7 +76,11 @@ enum {
   MOE_FLAG_RENORM_SURVIVORS = 1u,
   /* A token whose picks were all dropped outputs x_t (the wiki pseudocode's
    * identity fallback). */
-  MOE_FLAG_IDENTITY_FALLBACK = 2u
+  MOE_FLAG_IDENTITY_FALLBACK = 2u,
+  /* The router also stores every token's full probability row and the
+   * logsumexp of its logits in the workspace (probs, lse), for
+   * moe_router_stats. Routing results are unchanged. */
+  MOE_FLAG_ROUTER_STATS = 8u
 };
 
 typedef struct {
@@ -116,6 +120,8 @@ typedef struct {
                        * configs, else per 256-row block) and an exit count, read by the fused expert
                        * FFN; zero between calls (moe_workspace_init, moe_dispatch and every
                        * completed moe_expert_ffn leave them zero) */
+  size_t probs;       /* fp32  [T, N]  MOE_FLAG_ROUTER_STATS only: p[t, e] for every expert */
+  size_t lse;         /* fp32  [T]     MOE_FLAG_ROUTER_STATS only: logsumexp of token t's logits */
   size_t total;       /* bytes of the whole workspace */
   int64_t rows;       /* R_max */
   int64_t capacity;   /* C */
@@ -157,6 +163,19 @@ moe_status moe_get_device_status(void *ws, moe_stream_t stream);
  *   ws: a workspace of cfg (its status word is used). */
 moe_status moe_route(const moe_config *cfg, const void *x, const void *w_g, const float *router_bias,
                      int32_t *topk_idx, float *gate, float *score, void *ws, moe_stream_t stream);
+
+/* Router statistics of the last routed batch ("Mixture-of-Experts" wiki, the
+ * load-balancing auxiliary loss; "Mixture of Experts (MoE): Architecture,
+ * Routing, and Scaling", "Importance Loss and Z-Loss"). Needs a workspace of
+ * a cfg with MOE_FLAG_ROUTER_STATS on which moe_route (or moe_forward) ran.
+ *   counts_raw [N] int32: requests per expert from moe_dispatch (router picks,
+ *   before capacity). Out (device, fp32): f [N] = counts_raw[e] / (T*k);
+ *   P [N] = mean over tokens of p[t, e]; losses [2] = {N * sum_e f[e] P[e]
+ *   (the auxiliary balance loss, 1 at a perfectly uniform split), mean over
+ *   tokens of logsumexp(logits)^2 (the z-loss)}. Sums run in a fixed order:
+ *   deterministic. MOE_ERR_INVALID_ARG without the flag. */
+moe_status moe_router_stats(const moe_config *cfg, void *ws, const int32_t *counts_raw, float *f, float *P,
+                            float *losses, moe_stream_t stream);
 
 /* Steps 4-5: capacity enforcement and dispatch. Per expert, keep the top C
  * requests by (score desc, token asc); number the kept rows of each expert in

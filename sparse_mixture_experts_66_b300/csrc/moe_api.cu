@@ -50,7 +50,7 @@ moe_status check_config(const moe_config *cfg, Dims *D) {
   if (cfg->d < 8 || cfg->d % mult || cfg->d_ff < 8 || cfg->d_ff % mult)
     return fail(MOE_ERR_INVALID_ARG, "d and d_ff must be >= 8 and multiples of %lld (got d=%lld d_ff=%lld)",
                 (long long)mult, (long long)cfg->d, (long long)cfg->d_ff);
-  if (cfg->flags & ~(uint32_t)(MOE_FLAG_RENORM_SURVIVORS | MOE_FLAG_IDENTITY_FALLBACK))
+  if (cfg->flags & ~(uint32_t)(MOE_FLAG_RENORM_SURVIVORS | MOE_FLAG_IDENTITY_FALLBACK | MOE_FLAG_ROUTER_STATS))
     return fail(MOE_ERR_INVALID_ARG, "unknown flag bits 0x%x", cfg->flags);
   if (isnan(cfg->capacity_factor)) return fail(MOE_ERR_INVALID_ARG, "capacity_factor is NaN");
   D->T = cfg->T;
@@ -95,6 +95,9 @@ void make_layout(const Dims &D, moe_workspace_layout *L) {
   const int S = decode_splits(D);
   L->y_split = take(S > 1 ? (size_t)(S - 1) * R * (size_t)D.d * 4 : 0);
   L->ffn_sync = take((size_t)ffn_sync_ints(D) * 4);
+  const bool stats = (D.flags & MOE_FLAG_ROUTER_STATS) != 0;
+  L->probs = take(stats ? (size_t)D.T * N * 4 : 0);
+  L->lse = take(stats ? (size_t)D.T * 4 : 0);
   L->total = off;
   L->rows = D.R_max;
   L->capacity = D.C;
@@ -124,9 +127,15 @@ moe_status check_opt(const void *p, const char *what) {
 moe_status do_route(const Dims &D, const moe_workspace_layout &L, const void *x, const void *w_g,
                     const float *router_bias, int32_t *topk_idx, float *gate, float *score, void *ws,
                     cudaStream_t s) {
+  // with MOE_FLAG_ROUTER_STATS the router also stores full probability rows and logsumexps
+  const bool stats = (D.flags & MOE_FLAG_ROUTER_STATS) != 0;
+  float *probs = stats ? AT(ws, L.probs, float *) : nullptr;
+  float *lse = stats ? AT(ws, L.lse, float *) : nullptr;
   cudaError_t e = D.dt == MOE_DT_BF16 && !router_split(D)
-                      ? launch_router_tc(D, x, w_g, router_bias, topk_idx, gate, score, AT(ws, L.status, int32_t *), s)
-                      : launch_router(D, x, w_g, router_bias, topk_idx, gate, score, AT(ws, L.status, int32_t *), s);
+                      ? launch_router_tc(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse,
+                                         AT(ws, L.status, int32_t *), s)
+                      : launch_router(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse,
+                                      AT(ws, L.status, int32_t *), s);
   if (e != cudaSuccess) return cuda_fail(e, "router launch");
   return MOE_OK;
 }
@@ -247,6 +256,21 @@ moe_status moe_route(const moe_config *cfg, const void *x, const void *w_g, cons
   moe_workspace_layout L;
   make_layout(D, &L);
   return do_route(D, L, x, w_g, router_bias, topk_idx, gate, score, ws, (cudaStream_t)stream);
+}
+
+moe_status moe_router_stats(const moe_config *cfg, void *ws, const int32_t *counts_raw, float *f, float *P,
+                            float *losses, moe_stream_t stream) {
+  Dims D;
+  TRY(check_config(cfg, &D));
+  if (!(D.flags & MOE_FLAG_ROUTER_STATS))
+    return fail(MOE_ERR_INVALID_ARG, "moe_router_stats: the config lacks MOE_FLAG_ROUTER_STATS");
+  TRY(check_ptrs({ws, counts_raw, f, P, losses}, "moe_router_stats"));
+  moe_workspace_layout L;
+  make_layout(D, &L);
+  cudaError_t e = launch_router_stats(D, AT(ws, L.probs, const float *), AT(ws, L.lse, const float *), counts_raw,
+                                      f, P, losses, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "router statistics launch");
+  return MOE_OK;
 }
 
 moe_status moe_dispatch(const moe_config *cfg, const void *x, const int32_t *topk_idx, const float *gate,

@@ -160,12 +160,21 @@ void set_last_error(const char *text);
 constexpr int64_t kSplitRouterMaxT = 1024;
 inline bool router_split(const Dims &D) { return D.T <= kSplitRouterMaxT; }
 
+// probs [T, N] and lse [T] (both NULL unless router statistics are on): every
+// token's full probability row and the logsumexp of its logits.
 cudaError_t launch_router(const Dims &D, const void *x, const void *w_g, const float *router_bias,
-                          int32_t *topk_idx, float *gate, float *score, int32_t *status, cudaStream_t s);
+                          int32_t *topk_idx, float *gate, float *score, float *probs, float *lse, int32_t *status,
+                          cudaStream_t s);
 
 // Router on the tensor cores (bf16 inputs, N <= 256); cudaErrorNotSupported otherwise.
 cudaError_t launch_router_tc(const Dims &D, const void *x, const void *w_g, const float *router_bias,
-                             int32_t *topk_idx, float *gate, float *score, int32_t *status, cudaStream_t s);
+                             int32_t *topk_idx, float *gate, float *score, float *probs, float *lse, int32_t *status,
+                             cudaStream_t s);
+
+// Router statistics from the stored probabilities (fixed-order reductions):
+// P [N] column means, losses[1] = mean lse^2, then f [N] and losses[0] = aux.
+cudaError_t launch_router_stats(const Dims &D, const float *probs, const float *lse, const int32_t *counts_raw,
+                                float *f, float *P, float *losses, cudaStream_t s);
 
 cudaError_t launch_capacity(const Dims &D, const int32_t *topk_idx, const float *gate, const float *score,
                             int32_t *counts_raw, int32_t *counts_kept, int32_t *offsets, uint32_t *sel_thr,

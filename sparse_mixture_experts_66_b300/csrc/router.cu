@@ -144,7 +144,9 @@ __global__ void __launch_bounds__(kWarps * 32) router_small_kernel(const T *__re
                                                                    const float *__restrict__ router_bias, int64_t T_,
                                                                    int d, int N, int k, int32_t *__restrict__ topk_idx,
                                                                    float *__restrict__ gate,
-                                                                   float *__restrict__ score) {
+                                                                   float *__restrict__ score,
+                                                                   float *__restrict__ probs,
+                                                                   float *__restrict__ lse) {
   pdl_wait();
   extern __shared__ uint4 s_w[];  // [N * d * sizeof(T) / 16]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -174,6 +176,10 @@ __global__ void __launch_bounds__(kWarps * 32) router_small_kernel(const T *__re
   float s = ex;
 #pragma unroll
   for (int off = 8; off >= 2; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
+  if (probs && t < T_) {  // router statistics (lanes L and L^1 hold the same expert)
+    if (valid && (lane & 1) == 0) probs[t * N + e] = ex / s;
+    if ((lane & 15) == 0) lse[t] = m + logf(s);
+  }
   bool taken = !valid;
   float sel_ex[8];
   int sel_e[8];
@@ -215,7 +221,8 @@ __global__ void __launch_bounds__(kWarps * 32) router_small_kernel(const T *__re
 // expert; the picks are written in rank order.
 __device__ __forceinline__ void finish_token(float (&lv)[8], const float *__restrict__ router_bias, int N, int k,
                                              int lane, int64_t t, int32_t *__restrict__ topk_idx,
-                                             float *__restrict__ gate, float *__restrict__ score) {
+                                             float *__restrict__ gate, float *__restrict__ score,
+                                             float *__restrict__ probs, float *__restrict__ lse) {
   float m = -INFINITY;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -235,6 +242,12 @@ __device__ __forceinline__ void finish_token(float (&lv)[8], const float *__rest
     if (lane + 32 * i < N) s += expf(lv[i] - m);
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
+  if (probs) {  // router statistics: the full probability row and the logsumexp
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (lane + 32 * i < N) probs[t * N + lane + 32 * i] = expf(lv[i] - m) / s;
+    if (lane == 0) lse[t] = m + logf(s);
+  }
   uint32_t taken = 0;
   float sel_ex[8];
   int sel_e[8];
@@ -284,7 +297,8 @@ template <typename T>
 __global__ void __launch_bounds__(kWarps * 32) router_kernel(const T *__restrict__ x, const T *__restrict__ w_g,
                                                              const float *__restrict__ router_bias, int64_t T_,
                                                              int d, int N, int k, int32_t *__restrict__ topk_idx,
-                                                             float *__restrict__ gate, float *__restrict__ score) {
+                                                             float *__restrict__ gate, float *__restrict__ score,
+                                                             float *__restrict__ probs, float *__restrict__ lse) {
   pdl_wait();
   extern __shared__ float s_logits[];  // [kTokPerBlock][N]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -307,7 +321,7 @@ __global__ void __launch_bounds__(kWarps * 32) router_kernel(const T *__restrict
     float lv[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) lv[i] = lane + 32 * i < N ? L[lane + 32 * i] : -INFINITY;
-    finish_token(lv, router_bias, N, k, lane, t, topk_idx, gate, score);
+    finish_token(lv, router_bias, N, k, lane, t, topk_idx, gate, score, probs, lse);
   }
 }
 
@@ -323,7 +337,9 @@ __global__ void __launch_bounds__(kWarps * 32) router_split_kernel(const T *__re
                                                                    int64_t T_, int d, int N, int k,
                                                                    int32_t *__restrict__ topk_idx,
                                                                    float *__restrict__ gate,
-                                                                   float *__restrict__ score) {
+                                                                   float *__restrict__ score,
+                                                                   float *__restrict__ probs,
+                                                                   float *__restrict__ lse) {
   pdl_wait();
   extern __shared__ float s_part[];  // [kWarps][kTokPerWarp][N]
   constexpr int V = VecN<T>::n;
@@ -354,7 +370,7 @@ __global__ void __launch_bounds__(kWarps * 32) router_split_kernel(const T *__re
           for (int w = 0; w < kWarps; ++w) v += s_part[(w * kTokPerWarp + warp) * N + e];
         lv[i] = v;
       }
-      finish_token(lv, router_bias, N, k, lane, t, topk_idx, gate, score);
+      finish_token(lv, router_bias, N, k, lane, t, topk_idx, gate, score, probs, lse);
     }
   }
 }
@@ -364,12 +380,13 @@ __global__ void __launch_bounds__(kWarps * 32) router_split_kernel(const T *__re
 // The three SIMT router kernels share one argument list.
 template <typename T>
 static cudaError_t launch_router_t(const Dims &D, const T *x, const T *w_g, const float *router_bias,
-                                   int32_t *topk_idx, float *gate, float *score, cudaStream_t s) {
+                                   int32_t *topk_idx, float *gate, float *score, float *probs, float *lse,
+                                   cudaStream_t s) {
   if (router_split(D)) {
     const unsigned g = (unsigned)((D.T + kTokPerWarp - 1) / kTokPerWarp);
     const size_t smem = sizeof(float) * kWarps * kTokPerWarp * D.N;
     return launch_k(router_split_kernel<T>, dim3(g), dim3(kWarps * 32), smem, s, 1u, x, w_g, router_bias, D.T,
-                    (int)D.d, D.N, D.k, topk_idx, gate, score);
+                    (int)D.d, D.N, D.k, topk_idx, gate, score, probs, lse);
   }
   const unsigned grid = (unsigned)((D.T + kTokPerBlock - 1) / kTokPerBlock);
   if (D.N <= kEC) {
@@ -382,20 +399,21 @@ static cudaError_t launch_router_t(const Dims &D, const T *x, const T *w_g, cons
       if (e != cudaSuccess) return e;
     }
     return launch_k(kern, dim3(grid), dim3(kWarps * 32), smem, s, 1u, x, w_g, router_bias, D.T, (int)D.d, D.N, D.k,
-                    topk_idx, gate, score);
+                    topk_idx, gate, score, probs, lse);
   }
   const size_t smem = sizeof(float) * kTokPerBlock * D.N;
   return launch_k(router_kernel<T>, dim3(grid), dim3(kWarps * 32), smem, s, 1u, x, w_g, router_bias, D.T, (int)D.d,
-                  D.N, D.k, topk_idx, gate, score);
+                  D.N, D.k, topk_idx, gate, score, probs, lse);
 }
 
 cudaError_t launch_router(const Dims &D, const void *x, const void *w_g, const float *router_bias,
-                          int32_t *topk_idx, float *gate, float *score, int32_t *status, cudaStream_t s) {
+                          int32_t *topk_idx, float *gate, float *score, float *probs, float *lse, int32_t *status,
+                          cudaStream_t s) {
   (void)status;
   if (D.dt == MOE_DT_BF16)
     return launch_router_t(D, (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)w_g, router_bias, topk_idx, gate,
-                           score, s);
-  return launch_router_t(D, (const float *)x, (const float *)w_g, router_bias, topk_idx, gate, score, s);
+                           score, probs, lse, s);
+  return launch_router_t(D, (const float *)x, (const float *)w_g, router_bias, topk_idx, gate, score, probs, lse, s);
 }
 
 }  // namespace moe

@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                      const float *__restrict__ router_bias, int64_t T_, int d, int N, int k,
                      int32_t *__restrict__ topk_idx, float *__restrict__ gate, float *__restrict__ score,
-                     int32_t *status) {
+                     float *__restrict__ probs, float *__restrict__ lse, int32_t *status) {
   using C = RCfg<NP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -211,6 +211,25 @@ __global__ void __launch_bounds__(kRThreads, 1)
           sum += expf(__uint_as_float(r[j]) + c->bias[e] - m);
         }
       }
+      if (probs) {  // router statistics: the full probability row and the logsumexp
+        // (the TMEM loads are warp-collective: every lane runs them, only
+        // lanes of real tokens store)
+#pragma unroll 1
+        for (int c0 = 0; c0 < NP; c0 += 32) {
+          uint32_t r[32];
+          __syncwarp();
+          tmem_ld32(lane_base + (uint32_t)c0, r);
+          if (t < T_) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int e = c0 + j;
+              if (e >= N) break;
+              probs[t * N + e] = expf(__uint_as_float(r[j]) + c->bias[e] - m) / sum;
+            }
+          }
+        }
+        if (t < T_) lse[t] = m + logf(sum);
+      }
       if (t < T_) {
         float ex[8], sel = 0.f;
 #pragma unroll
@@ -241,7 +260,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
 
 template <int NP>
 cudaError_t launch_np(const Dims &D, const void *x, const void *w_g, const float *router_bias, int32_t *topk_idx,
-                      float *gate, float *score, int32_t *status, cudaStream_t s) {
+                      float *gate, float *score, float *probs, float *lse, int32_t *status, cudaStream_t s) {
   static bool attr_set = false;
   const size_t smem = router_smem<NP>();
   if (!attr_set) {
@@ -256,19 +275,20 @@ cudaError_t launch_np(const Dims &D, const void *x, const void *w_g, const float
   if (!make_map(&tx, x, 2, dx, kRM) || !make_map(&tw, w_g, 2, dw, NP)) return cudaErrorInvalidValue;
   const unsigned grid = (unsigned)((D.T + kRM - 1) / kRM);
   return launch_k(router_tc_kernel<NP>, dim3(grid), dim3(kRThreads), smem, s, 1u, tx, tw, router_bias, D.T, (int)D.d,
-                  D.N, D.k, topk_idx, gate, score, status);
+                  D.N, D.k, topk_idx, gate, score, probs, lse, status);
 }
 
 }  // namespace
 
 cudaError_t launch_router_tc(const Dims &D, const void *x, const void *w_g, const float *router_bias,
-                             int32_t *topk_idx, float *gate, float *score, int32_t *status, cudaStream_t s) {
+                             int32_t *topk_idx, float *gate, float *score, float *probs, float *lse, int32_t *status,
+                             cudaStream_t s) {
   if (D.dt != MOE_DT_BF16 || D.N > 256) return cudaErrorNotSupported;
-  if (D.N <= 16) return launch_np<16>(D, x, w_g, router_bias, topk_idx, gate, score, status, s);
-  if (D.N <= 32) return launch_np<32>(D, x, w_g, router_bias, topk_idx, gate, score, status, s);
-  if (D.N <= 64) return launch_np<64>(D, x, w_g, router_bias, topk_idx, gate, score, status, s);
-  if (D.N <= 128) return launch_np<128>(D, x, w_g, router_bias, topk_idx, gate, score, status, s);
-  return launch_np<256>(D, x, w_g, router_bias, topk_idx, gate, score, status, s);
+  if (D.N <= 16) return launch_np<16>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
+  if (D.N <= 32) return launch_np<32>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
+  if (D.N <= 64) return launch_np<64>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
+  if (D.N <= 128) return launch_np<128>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
+  return launch_np<256>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
 }
 
 }  // namespace moe

@@ -34,6 +34,7 @@ MOE_DT_F32 = 0
 MOE_DT_BF16 = 1
 MOE_FLAG_RENORM_SURVIVORS = 1
 MOE_FLAG_IDENTITY_FALLBACK = 2
+MOE_FLAG_ROUTER_STATS = 8
 
 _DT_CODE = {torch.float32: MOE_DT_F32, torch.bfloat16: MOE_DT_BF16}
 _DT_TORCH = {MOE_DT_F32: torch.float32, MOE_DT_BF16: torch.bfloat16}
@@ -58,7 +59,7 @@ class MoeConfig(ctypes.Structure):
 class MoeWorkspaceLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "status", "topk_idx", "gate", "score", "counts_raw", "counts_kept", "offsets", "sel_thr", "sel_eq",
-        "row_of", "row_token", "row_gate", "x_perm", "h", "y_perm", "y_split", "ffn_sync", "total")] + [
+        "row_of", "row_token", "row_gate", "x_perm", "h", "y_perm", "y_split", "ffn_sync", "probs", "lse", "total")] + [
         ("rows", ctypes.c_int64), ("capacity", ctypes.c_int64)]
 
 
@@ -78,6 +79,7 @@ SIGNATURES = {
     "moe_combine": (["C"] + ["P"] * 6 + ["S"], ctypes.c_int),
     "moe_forward": (["C"] + ["P"] * 9 + ["S"], ctypes.c_int),
     "moe_forward_noalloc": (["C"] + ["P"] * 8 + ["S"], ctypes.c_int),
+    "moe_router_stats": (["C"] + ["P"] * 5 + ["S"], ctypes.c_int),
 }
 _KIND = {"C": ctypes.POINTER(MoeConfig), "P": ctypes.c_void_p, "S": ctypes.c_void_p,
          "L": ctypes.POINTER(MoeWorkspaceLayout)}
@@ -175,6 +177,11 @@ def moe_route(cfg, x, w_g, router_bias, topk_idx, gate, score, ws, stream=None):
                             _ptr(score), _ptr(ws), _stream(stream)))
 
 
+def moe_router_stats(cfg, ws, counts_raw, f, P, losses, stream=None):
+    _check(load().moe_router_stats(ctypes.byref(cfg), _ptr(ws), _ptr(counts_raw), _ptr(f), _ptr(P), _ptr(losses),
+                                   _stream(stream)))
+
+
 def moe_dispatch(cfg, x, topk_idx, gate, score, counts_raw, counts_kept, offsets, row_of, row_token, row_gate,
                  x_perm, ws, stream=None):
     _check(load().moe_dispatch(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(gate), _ptr(score),
@@ -236,7 +243,9 @@ class Workspace:
             row_token=self.view("row_token", torch.int32, (R,)), row_gate=self.view("row_gate", torch.float32, (R,)),
             x_perm=self.view("x_perm", dt, (R, c.d)), h=self.view("h", dt, (R, c.d_ff)),
             y_perm=self.view("y_perm", torch.float32, (R, c.d)),
-            y_split=self.view("y_split", torch.float32, (self.splits - 1, R, c.d)))
+            y_split=self.view("y_split", torch.float32, (self.splits - 1, R, c.d)),
+            probs=self.view("probs", torch.float32, (T, N) if c.flags & MOE_FLAG_ROUTER_STATS else (0, N)),
+            lse=self.view("lse", torch.float32, (T,) if c.flags & MOE_FLAG_ROUTER_STATS else (0,)))
 
     @property
     def splits(self):

@@ -72,7 +72,7 @@ def test_workspace_layout_is_aligned_and_sized():
         L = moe.moe_get_workspace_layout(cfg)
         S = min(w.T * w.k, w.N * L.capacity)
         assert L.rows == (S + 127 * w.N) // 128 * 128
-        offs = [getattr(L, f) for f, _ in moe.MoeWorkspaceLayout._fields_[:17]]
+        offs = [getattr(L, f) for f, _ in moe.MoeWorkspaceLayout._fields_[:19]]
         assert all(o % 256 == 0 for o in offs)
         assert offs == sorted(offs)
         es = 2 if w.dtype == "bf16" else 4
@@ -82,7 +82,7 @@ def test_workspace_layout_is_aligned_and_sized():
 
 
 @pytest.mark.parametrize("field,value", [("T", 0), ("N", 0), ("N", 257), ("k", 0), ("k", 9), ("d", 12),
-                                         ("d_ff", 4), ("dtype", 7), ("flags", 8)])
+                                         ("d_ff", 4), ("dtype", 7), ("flags", 16)])
 def test_invalid_config_rejected_on_host(field, value):
     cfg = moe.make_config(64, 64, 64, 8, 2, 1.25)
     setattr(cfg, field, value)
@@ -123,6 +123,23 @@ def test_flag_variants_need_their_inputs():
     cfg.flags = moe.MOE_FLAG_IDENTITY_FALLBACK
     st = lib.moe_combine(ctypes.byref(cfg), p, p, None, None, p, p, None)
     assert st == moe.MOE_ERR_INVALID_ARG and b"x" in lib.moe_last_error()
+
+
+def test_router_stats_need_their_flag_and_buffers():
+    """moe_router_stats reads what the router stored under MOE_FLAG_ROUTER_STATS;
+    without the flag (or with a missing output) it is rejected on the host."""
+    lib = moe.load()
+    p = ctypes.c_void_p(0x1000)
+    cfg = moe.make_config(64, 64, 64, 8, 2, 1.25)
+    st = lib.moe_router_stats(ctypes.byref(cfg), p, p, p, p, p, None)
+    assert st == moe.MOE_ERR_INVALID_ARG and b"MOE_FLAG_ROUTER_STATS" in lib.moe_last_error()
+    cfg.flags = moe.MOE_FLAG_ROUTER_STATS
+    st = lib.moe_router_stats(ctypes.byref(cfg), p, p, p, None, p, None)
+    assert st == moe.MOE_ERR_INVALID_ARG and b"NULL" in lib.moe_last_error()
+    # the statistics buffers exist in the workspace only under the flag
+    L0 = moe.moe_get_workspace_layout(moe.make_config(64, 64, 64, 8, 2, 1.25))
+    L1 = moe.moe_get_workspace_layout(cfg)
+    assert L0.lse == L0.probs and L1.lse - L1.probs >= 64 * 8 * 4 and L1.total - L1.lse >= 64 * 4
 
 
 def test_binding_refuses_cpu_tensors():

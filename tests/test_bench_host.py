@@ -27,7 +27,7 @@ def _rank_main(rank, world, port, out):
 
 def test_replica_throughput_takes_the_slowest_rank():
     port = 29500 + os.getpid() % 1000
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_rank_main, args=(2, port, out), nprocs=2, join=True)
         res = dict(out)

@@ -246,3 +246,57 @@ def test_full_size_workloads(name):
     rep, g, ref, _ = parity.full_check(w, sample=48)
     print(name, rep)
     torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
+# Router statistics (MOE_FLAG_ROUTER_STATS + moe_router_stats)
+# ---------------------------------------------------------------------------
+STATS_CASES = [
+    custom(2048, 256, 64, 8, 2, 1.25, seed=21),  # bf16, tensor-core router
+    custom(1500, 128, 64, 64, 2, 1.0, router_bias="zipf", seed=22),  # bf16, tensor-core router, N=64 + bias
+    custom(300, 128, 64, 16, 4, math.inf, seed=23),  # bf16, split-column router
+    custom(1200, 64, 64, 4, 1, 1.25, dtype="f32", seed=24),  # fp32, N <= 8 register router
+    custom(1100, 64, 64, 40, 3, 1.0, dtype="f32", seed=25),  # fp32, generic router
+]
+
+
+@pytest.mark.parametrize("w", STATS_CASES, ids=lambda w: w.name)
+def test_router_stats_against_oracle(w):
+    """Stored probability rows, f_e, P_e, the auxiliary loss and the z-loss
+    against the oracle. f_e comes from the GPU's own picks (compared exactly);
+    P_e, aux and z within 2e-5 relative (fp32 against fp64)."""
+    inp = draw(w)
+    g = parity.run_gpu(w, inp, flags=moe.MOE_FLAG_ROUTER_STATS)
+    cfg, ws = g["_cfg"], g["_ws"]
+    v = ws.views()
+    f = torch.empty(w.N, dtype=torch.float32, device="cuda")
+    P = torch.empty(w.N, dtype=torch.float32, device="cuda")
+    losses = torch.empty(2, dtype=torch.float32, device="cuda")
+    moe.moe_router_stats(cfg, ws.buf, v["counts_raw"], f, P, losses)
+    ws.status()
+    probs = v["probs"].cpu().numpy().astype(np.float64)
+    ref = parity.oracle_ref(w, inp, sel=np.array([0]))
+    # the stored rows are the softmax of the fp32 logits; the picks' rows equal their scores exactly
+    assert np.max(np.abs(probs - ref["probs"])) <= 2e-5
+    assert np.allclose(probs.sum(axis=1), 1.0, atol=1e-5)
+    picked = np.take_along_axis(v["probs"].cpu().numpy(), g["topk_idx"].astype(np.int64), axis=1)
+    assert np.array_equal(picked, g["score"])
+    # the oracle's statistics on the GPU's own picks
+    f_ref, P_ref, aux_ref, z_ref = O.load().router_stats(ref["logits"], ref["probs"], g["topk_idx"])
+    assert np.array_equal(f.cpu().numpy(), (g["counts_raw"] / np.float32(w.T * w.k)).astype(np.float32))
+    assert np.allclose(f.cpu().numpy(), f_ref, rtol=1e-6, atol=0)
+    assert np.allclose(P.cpu().numpy(), P_ref, rtol=2e-5, atol=1e-7)
+    aux, z = losses.cpu().numpy().astype(np.float64)
+    assert abs(aux - aux_ref) <= 2e-5 * aux_ref
+    assert abs(z - z_ref) <= 2e-5 * z_ref
+
+
+def test_router_stats_leave_routing_unchanged():
+    """The statistics flag changes no routing or output bit."""
+    w = STATS_CASES[1]
+    inp = draw(w)
+    a = parity.run_gpu(w, inp)
+    b = parity.run_gpu(w, inp, flags=moe.MOE_FLAG_ROUTER_STATS)
+    for key in ("topk_idx", "gate", "score", "row_of", "offsets"):
+        assert np.array_equal(a[key], b[key]), key
+    assert torch.equal(a["_y"], b["_y"])
