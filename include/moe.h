@@ -77,6 +77,12 @@ enum {
   /* A token whose picks were all dropped outputs x_t (the wiki pseudocode's
    * identity fallback). */
   MOE_FLAG_IDENTITY_FALLBACK = 2u,
+  /* An always-active shared expert (its own W1, b1, W2, b2 with the same
+   * d_ff) is added to every token's output after the routed sum ("Mixture of
+   * Experts: Scaling Language Models with Sparse Activation", "Comparing MoE
+   * Architectures": shared experts). Run moe_shared_expert before
+   * moe_combine, or moe_forward_shared. */
+  MOE_FLAG_SHARED_EXPERT = 4u,
   /* The router also stores every token's full probability row and the
    * logsumexp of its logits in the workspace (probs, lse), for
    * moe_router_stats. Routing results are unchanged. */
@@ -122,6 +128,11 @@ typedef struct {
                        * completed moe_expert_ffn leave them zero) */
   size_t probs;       /* fp32  [T, N]  MOE_FLAG_ROUTER_STATS only: p[t, e] for every expert */
   size_t lse;         /* fp32  [T]     MOE_FLAG_ROUTER_STATS only: logsumexp of token t's logits */
+  size_t shared_offsets; /* int32 [2]  MOE_FLAG_SHARED_EXPERT only: the shared expert's one segment */
+  size_t h_shared;    /* dtype [Tp, d_ff] MOE_FLAG_SHARED_EXPERT only: its hidden activations, Tp = T
+                       * rounded up to 128 */
+  size_t y_shared;    /* fp32  [Tp, d]    MOE_FLAG_SHARED_EXPERT only: its output */
+  size_t shared_sync; /* int32        MOE_FLAG_SHARED_EXPERT only: completion counters of its FFN */
   size_t total;       /* bytes of the whole workspace */
   int64_t rows;       /* R_max */
   int64_t capacity;   /* C */
@@ -209,6 +220,14 @@ moe_status moe_expert_ffn(const moe_config *cfg, const void *x_perm, const int32
                           const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
                           float *y_perm, void *ws, moe_stream_t stream);
 
+/* The shared expert over every token: y_shared[t] = W2s GELU(W1s x_t + b1s)
+ * + b2s into the workspace of a cfg with MOE_FLAG_SHARED_EXPERT (x [T, d],
+ * sw1 [d_ff, d], sb1 [d_ff], sw2 [d, d_ff], sb2 [d], all in dtype). Same
+ * arithmetic as moe_expert_ffn (one expert whose segment is the whole batch,
+ * unscaled); moe_combine then adds it. */
+moe_status moe_shared_expert(const moe_config *cfg, const void *x, const void *sw1, const void *sb1,
+                             const void *sw2, const void *sb2, void *ws, moe_stream_t stream);
+
 /* Step 7: y[t] = sum over j < k with row_of[t,j] >= 0, in j order, of
  * y_perm[row_of[t,j]], in fp32, stored in dtype. No atomics. For
  * decode-shaped configs each pick's term is first completed with the same row
@@ -216,9 +235,17 @@ moe_status moe_expert_ffn(const moe_config *cfg, const void *x_perm, const int32
  *   gate [T, k] is read only under MOE_FLAG_RENORM_SURVIVORS (the sum is then
  *   divided by the token's kept-gate sum); x [T, d] only under
  *   MOE_FLAG_IDENTITY_FALLBACK (a token with no kept pick outputs x_t). Either
- *   may be NULL otherwise. ws: a workspace of cfg (status word). */
+ *   may be NULL otherwise. Under MOE_FLAG_SHARED_EXPERT the workspace's
+ *   y_shared row is added last. ws: a workspace of cfg (status word). */
 moe_status moe_combine(const moe_config *cfg, const float *y_perm, const int32_t *row_of, const float *gate,
                        const void *x, void *y, void *ws, moe_stream_t stream);
+
+/* moe_forward plus the shared expert (cfg must carry MOE_FLAG_SHARED_EXPERT):
+ * route, dispatch, the routed expert FFNs, moe_shared_expert, combine. */
+moe_status moe_forward_shared(const moe_config *cfg, const void *x, const void *w_g, const float *router_bias,
+                              const void *w1, const void *b1, const void *w2, const void *b2, const void *sw1,
+                              const void *sb1, const void *sw2, const void *sb2, void *y, void *ws,
+                              moe_stream_t stream);
 
 /* The whole layer forward: moe_route, moe_dispatch, moe_expert_ffn and
  * moe_combine on the workspace's buffers, y [T, d] in dtype. After the

@@ -16,7 +16,7 @@ namespace {
 constexpr int BM = 64, BN = 64, BK = 16;
 
 template <typename Tin, typename Tout, int EPI>
-__global__ void __launch_bounds__(256) ffn_simt_kernel(const Tin *__restrict__ A, int64_t K,
+__global__ void __launch_bounds__(256) ffn_simt_kernel(const Tin *__restrict__ A, int64_t a_rows, int64_t K,
                                                        const Tin *__restrict__ B, const Tin *__restrict__ bias,
                                                        int64_t N_out, const float *__restrict__ row_gate,
                                                        const int32_t *__restrict__ offsets, int N_exp,
@@ -42,7 +42,7 @@ __global__ void __launch_bounds__(256) ffn_simt_kernel(const Tin *__restrict__ A
       const int l = tid + q * 256;
       const int r = l / BK, c = l % BK;
       const int64_t kk = k0 + c;
-      As[c][r] = kk < K ? to_f32(A[(m0 + r) * K + kk]) : 0.f;
+      As[c][r] = (kk < K && m0 + r < a_rows) ? to_f32(A[(m0 + r) * K + kk]) : 0.f;
       const int64_t n = n0 + r;
       Bs[c][r] = (kk < K && n < N_out) ? to_f32(Be[n * K + kk]) : 0.f;
     }
@@ -80,20 +80,20 @@ __global__ void __launch_bounds__(256) ffn_simt_kernel(const Tin *__restrict__ A
 
 }  // namespace
 
-cudaError_t launch_ffn_simt(const Dims &D, int epi, const void *A, int64_t K, const void *B, const void *bias,
-                            int64_t N_out, const float *row_gate, const int32_t *offsets, void *out,
+cudaError_t launch_ffn_simt(const Dims &D, int epi, const void *A, int64_t a_rows, int64_t K, const void *B,
+                            const void *bias, int64_t N_out, const float *row_gate, const int32_t *offsets, void *out,
                             int32_t *status, cudaStream_t s) {
   (void)status;
   const dim3 grid((unsigned)((N_out + BN - 1) / BN), (unsigned)(D.R_max / BM));
   if (D.dt == MOE_DT_F32)
     return launch_k(epi == 1 ? ffn_simt_kernel<float, float, 1> : ffn_simt_kernel<float, float, 2>, grid, dim3(256),
-                    0, s, 1u, (const float *)A, K, (const float *)B, (const float *)bias, N_out, row_gate, offsets,
+                    0, s, 1u, (const float *)A, a_rows, K, (const float *)B, (const float *)bias, N_out, row_gate, offsets,
                     D.N, (float *)out);
   if (epi == 1)
     return launch_k(ffn_simt_kernel<__nv_bfloat16, __nv_bfloat16, 1>, grid, dim3(256), 0, s, 1u,
-                    (const __nv_bfloat16 *)A, K, (const __nv_bfloat16 *)B, (const __nv_bfloat16 *)bias, N_out,
+                    (const __nv_bfloat16 *)A, a_rows, K, (const __nv_bfloat16 *)B, (const __nv_bfloat16 *)bias, N_out,
                     row_gate, offsets, D.N, (__nv_bfloat16 *)out);
-  return launch_k(ffn_simt_kernel<__nv_bfloat16, float, 2>, grid, dim3(256), 0, s, 1u, (const __nv_bfloat16 *)A, K,
+  return launch_k(ffn_simt_kernel<__nv_bfloat16, float, 2>, grid, dim3(256), 0, s, 1u, (const __nv_bfloat16 *)A, a_rows, K,
                   (const __nv_bfloat16 *)B, (const __nv_bfloat16 *)bias, N_out, row_gate, offsets, D.N,
                   (float *)out);
 }

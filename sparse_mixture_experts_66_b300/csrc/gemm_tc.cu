@@ -546,9 +546,9 @@ int resident_pairs() {
 
 }  // namespace
 
-cudaError_t launch_ffn_tc(const Dims &D, const void *x_perm, const int32_t *offsets, const void *w1, const void *b1,
-                          const void *w2, const void *b2, const float *row_gate, void *h, float *y_perm,
-                          int32_t *blk_done, int32_t *status, cudaStream_t s) {
+cudaError_t launch_ffn_tc(const Dims &D, const void *x_perm, int64_t a_rows, const int32_t *offsets, const void *w1,
+                          const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
+                          float *y_perm, int32_t *blk_done, int32_t *status, cudaStream_t s) {
   if (D.dt != MOE_DT_BF16 || D.N > kMaxExperts || D.d > (1 << 30) || D.d_ff > (1 << 30) || !blk_done)
     return cudaErrorNotSupported;
   static bool attr_set = false;
@@ -558,7 +558,7 @@ cudaError_t launch_ffn_tc(const Dims &D, const void *x_perm, const int32_t *offs
     attr_set = true;
   }
   CUtensorMap tx, tw1, th, tw2;
-  const uint64_t dx[2] = {(uint64_t)D.d, (uint64_t)D.R_max};
+  const uint64_t dx[2] = {(uint64_t)D.d, (uint64_t)a_rows};  // rows past a_rows read as zeros
   const uint64_t dw1[3] = {(uint64_t)D.d, (uint64_t)D.d_ff, (uint64_t)D.N};
   const uint64_t dh[2] = {(uint64_t)D.d_ff, (uint64_t)D.R_max};
   const uint64_t dw2[3] = {(uint64_t)D.d_ff, (uint64_t)D.d, (uint64_t)D.N};

@@ -50,7 +50,8 @@ moe_status check_config(const moe_config *cfg, Dims *D) {
   if (cfg->d < 8 || cfg->d % mult || cfg->d_ff < 8 || cfg->d_ff % mult)
     return fail(MOE_ERR_INVALID_ARG, "d and d_ff must be >= 8 and multiples of %lld (got d=%lld d_ff=%lld)",
                 (long long)mult, (long long)cfg->d, (long long)cfg->d_ff);
-  if (cfg->flags & ~(uint32_t)(MOE_FLAG_RENORM_SURVIVORS | MOE_FLAG_IDENTITY_FALLBACK | MOE_FLAG_ROUTER_STATS))
+  if (cfg->flags & ~(uint32_t)(MOE_FLAG_RENORM_SURVIVORS | MOE_FLAG_IDENTITY_FALLBACK | MOE_FLAG_ROUTER_STATS |
+                               MOE_FLAG_SHARED_EXPERT))
     return fail(MOE_ERR_INVALID_ARG, "unknown flag bits 0x%x", cfg->flags);
   if (isnan(cfg->capacity_factor)) return fail(MOE_ERR_INVALID_ARG, "capacity_factor is NaN");
   D->T = cfg->T;
@@ -67,6 +68,17 @@ moe_status check_config(const moe_config *cfg, Dims *D) {
   D->flags = cfg->flags;
   return MOE_OK;
 }
+
+// The shared expert as a one-expert FFN whose segment is the whole batch,
+// rounded up to 128 rows.
+Dims shared_dims(const Dims &D) {
+  Dims S1 = D;
+  S1.N = 1;
+  S1.k = 1;
+  S1.R_max = (D.T + kRowAlign - 1) / kRowAlign * kRowAlign;
+  return S1;
+}
+int64_t shared_sync_ints(const Dims &D) { return ffn_blocks_max(shared_dims(D)) + 1; }
 
 void make_layout(const Dims &D, moe_workspace_layout *L) {
   const size_t es = D.dt == MOE_DT_BF16 ? 2 : 4;
@@ -98,6 +110,12 @@ void make_layout(const Dims &D, moe_workspace_layout *L) {
   const bool stats = (D.flags & MOE_FLAG_ROUTER_STATS) != 0;
   L->probs = take(stats ? (size_t)D.T * N * 4 : 0);
   L->lse = take(stats ? (size_t)D.T * 4 : 0);
+  const bool shared = (D.flags & MOE_FLAG_SHARED_EXPERT) != 0;
+  const Dims S1 = shared_dims(D);
+  L->shared_offsets = take(shared ? 8 : 0);
+  L->h_shared = take(shared ? (size_t)S1.R_max * (size_t)D.d_ff * es : 0);
+  L->y_shared = take(shared ? (size_t)S1.R_max * (size_t)D.d * 4 : 0);
+  L->shared_sync = take(shared ? (size_t)shared_sync_ints(D) * 4 : 0);
   L->total = off;
   L->rows = D.R_max;
   L->capacity = D.C;
@@ -167,16 +185,16 @@ moe_status do_ffn(const Dims &D, const moe_workspace_layout &L, const void *x_pe
     return MOE_OK;
   }
   if (D.dt == MOE_DT_BF16) {
-    cudaError_t e = launch_ffn_tc(D, x_perm, offsets, w1, b1, w2, b2, row_gate, h, y_perm,
+    cudaError_t e = launch_ffn_tc(D, x_perm, D.R_max, offsets, w1, b1, w2, b2, row_gate, h, y_perm,
                                   AT(ws, L.ffn_sync, int32_t *), status, s);
     if (e == cudaErrorNotSupported)
       return fail(MOE_ERR_UNSUPPORTED, "expert FFN: shape not supported by the tensor-core kernels");
     if (e != cudaSuccess) return cuda_fail(e, "expert FFN (tensor cores)");
     return MOE_OK;
   }
-  cudaError_t e = launch_ffn_simt(D, 1, x_perm, D.d, w1, b1, D.d_ff, nullptr, offsets, h, status, s);
+  cudaError_t e = launch_ffn_simt(D, 1, x_perm, D.R_max, D.d, w1, b1, D.d_ff, nullptr, offsets, h, status, s);
   if (e != cudaSuccess) return cuda_fail(e, "expert GEMM1 launch");
-  e = launch_ffn_simt(D, 2, h, D.d_ff, w2, b2, D.d, row_gate, offsets, y_perm, status, s);
+  e = launch_ffn_simt(D, 2, h, D.R_max, D.d_ff, w2, b2, D.d, row_gate, offsets, y_perm, status, s);
   if (e != cudaSuccess) return cuda_fail(e, "expert GEMM2 launch");
   return MOE_OK;
 }
@@ -184,9 +202,34 @@ moe_status do_ffn(const Dims &D, const moe_workspace_layout &L, const void *x_pe
 moe_status do_combine(const Dims &D, const moe_workspace_layout &L, const float *y_perm, const int32_t *row_of,
                       const float *gate, const void *x, void *y, void *ws, cudaStream_t s) {
   const int S = decode_splits(D);
+  const float *y_shared = (D.flags & MOE_FLAG_SHARED_EXPERT) ? AT(ws, L.y_shared, const float *) : nullptr;
   cudaError_t e = launch_combine(D, y_perm, S > 1 ? AT(ws, L.y_split, const float *) : nullptr, S > 1 ? S - 1 : 0,
-                                 row_of, gate, x, y, AT(ws, L.status, int32_t *), s);
+                                 row_of, gate, x, y_shared, y, AT(ws, L.status, int32_t *), s);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  return MOE_OK;
+}
+
+// The shared expert's FFN over x (T rows; TMA or the SIMT loads zero-fill the
+// rows up to the 128-row multiple) into the workspace's y_shared.
+moe_status do_shared(const Dims &D, const moe_workspace_layout &L, const void *x, const void *sw1, const void *sb1,
+                     const void *sw2, const void *sb2, void *ws, cudaStream_t s) {
+  const Dims S1 = shared_dims(D);
+  int32_t *status = AT(ws, L.status, int32_t *);
+  int32_t *offs = AT(ws, L.shared_offsets, int32_t *);
+  void *h = AT(ws, L.h_shared, void *);
+  float *y_sh = AT(ws, L.y_shared, float *);
+  cudaError_t e = launch_shared_setup(offs, S1.R_max, AT(ws, L.shared_sync, int32_t *), shared_sync_ints(D), s);
+  if (e != cudaSuccess) return cuda_fail(e, "shared expert setup");
+  if (D.dt == MOE_DT_BF16) {
+    e = launch_ffn_tc(S1, x, D.T, offs, sw1, sb1, sw2, sb2, nullptr, h, y_sh, AT(ws, L.shared_sync, int32_t *),
+                      status, s);
+    if (e != cudaSuccess) return cuda_fail(e, "shared expert FFN (tensor cores)");
+    return MOE_OK;
+  }
+  e = launch_ffn_simt(S1, 1, x, D.T, D.d, sw1, sb1, D.d_ff, nullptr, offs, h, status, s);
+  if (e != cudaSuccess) return cuda_fail(e, "shared expert GEMM1 launch");
+  e = launch_ffn_simt(S1, 2, h, S1.R_max, D.d_ff, sw2, sb2, D.d, nullptr, offs, y_sh, status, s);
+  if (e != cudaSuccess) return cuda_fail(e, "shared expert GEMM2 launch");
   return MOE_OK;
 }
 
@@ -314,11 +357,26 @@ moe_status moe_combine(const moe_config *cfg, const float *y_perm, const int32_t
   return do_combine(D, L, y_perm, row_of, gate, x, y, ws, (cudaStream_t)stream);
 }
 
+moe_status moe_shared_expert(const moe_config *cfg, const void *x, const void *sw1, const void *sb1,
+                             const void *sw2, const void *sb2, void *ws, moe_stream_t stream) {
+  Dims D;
+  TRY(check_config(cfg, &D));
+  if (!(D.flags & MOE_FLAG_SHARED_EXPERT))
+    return fail(MOE_ERR_INVALID_ARG, "moe_shared_expert: the config lacks MOE_FLAG_SHARED_EXPERT");
+  TRY(check_ptrs({x, sw1, sb1, sw2, sb2, ws}, "moe_shared_expert"));
+  moe_workspace_layout L;
+  make_layout(D, &L);
+  return do_shared(D, L, x, sw1, sb1, sw2, sb2, ws, (cudaStream_t)stream);
+}
+
 moe_status moe_forward(const moe_config *cfg, const void *x, const void *w_g, const float *router_bias,
                        const void *w1, const void *b1, const void *w2, const void *b2, void *y, void *ws,
                        moe_stream_t stream) {
   Dims D;
   TRY(check_config(cfg, &D));
+  if (D.flags & MOE_FLAG_SHARED_EXPERT)
+    return fail(MOE_ERR_INVALID_ARG, "moe_forward: MOE_FLAG_SHARED_EXPERT needs the shared weights "
+                                     "(use moe_forward_shared)");
   TRY(check_ptrs({x, w_g, w1, b1, w2, b2, y, ws}, "moe_forward"));
   TRY(check_opt(router_bias, "moe_forward router_bias"));
   moe_workspace_layout L;
@@ -336,6 +394,36 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const void *w_g, co
   TRY(do_dispatch(D, L, x, topk_idx, gate, score, AT(ws, L.counts_raw, int32_t *), AT(ws, L.counts_kept, int32_t *),
                   offsets, row_of, AT(ws, L.row_token, int32_t *), row_gate, x_perm, ws, s));
   TRY(do_ffn(D, L, x_perm, offsets, w1, b1, w2, b2, row_gate, AT(ws, L.h, void *), y_perm, ws, s));
+  TRY(do_combine(D, L, y_perm, row_of, gate, x, y, ws, s));
+  return MOE_OK;
+}
+
+moe_status moe_forward_shared(const moe_config *cfg, const void *x, const void *w_g, const float *router_bias,
+                              const void *w1, const void *b1, const void *w2, const void *b2, const void *sw1,
+                              const void *sb1, const void *sw2, const void *sb2, void *y, void *ws,
+                              moe_stream_t stream) {
+  Dims D;
+  TRY(check_config(cfg, &D));
+  if (!(D.flags & MOE_FLAG_SHARED_EXPERT))
+    return fail(MOE_ERR_INVALID_ARG, "moe_forward_shared: the config lacks MOE_FLAG_SHARED_EXPERT");
+  TRY(check_ptrs({x, w_g, w1, b1, w2, b2, sw1, sb1, sw2, sb2, y, ws}, "moe_forward_shared"));
+  TRY(check_opt(router_bias, "moe_forward_shared router_bias"));
+  moe_workspace_layout L;
+  make_layout(D, &L);
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t *topk_idx = AT(ws, L.topk_idx, int32_t *);
+  float *gate = AT(ws, L.gate, float *);
+  float *score = AT(ws, L.score, float *);
+  int32_t *offsets = AT(ws, L.offsets, int32_t *);
+  int32_t *row_of = AT(ws, L.row_of, int32_t *);
+  float *row_gate = AT(ws, L.row_gate, float *);
+  void *x_perm = AT(ws, L.x_perm, void *);
+  float *y_perm = AT(ws, L.y_perm, float *);
+  TRY(do_route(D, L, x, w_g, router_bias, topk_idx, gate, score, ws, s));
+  TRY(do_dispatch(D, L, x, topk_idx, gate, score, AT(ws, L.counts_raw, int32_t *), AT(ws, L.counts_kept, int32_t *),
+                  offsets, row_of, AT(ws, L.row_token, int32_t *), row_gate, x_perm, ws, s));
+  TRY(do_ffn(D, L, x_perm, offsets, w1, b1, w2, b2, row_gate, AT(ws, L.h, void *), y_perm, ws, s));
+  TRY(do_shared(D, L, x, sw1, sb1, sw2, sb2, ws, s));
   TRY(do_combine(D, L, y_perm, row_of, gate, x, y, ws, s));
   return MOE_OK;
 }

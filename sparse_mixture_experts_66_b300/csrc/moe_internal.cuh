@@ -200,15 +200,17 @@ cudaError_t launch_permute(const Dims &D, const void *x, const int32_t *offsets,
 
 // y_split / nsplit: the extra K slices of a decode-mode second GEMM (nsplit
 // buffers of [R_max, d] after y_perm's own), added in slice order.
+// y_shared [Tp, d] fp32 or NULL: the shared expert's output, added last.
 cudaError_t launch_combine(const Dims &D, const float *y_perm, const float *y_split, int nsplit,
-                           const int32_t *row_of, const float *gate, const void *x, void *y, int32_t *status,
-                           cudaStream_t s);
+                           const int32_t *row_of, const float *gate, const void *x, const float *y_shared, void *y,
+                           int32_t *status, cudaStream_t s);
 
 // Grouped GEMM over expert segments with the two fused epilogues.
 //   epi 1: out[r, n] = GELU(A[r] . B[e, n] + bias[e, n])            (dtype)
 //   epi 2: out[r, n] = row_gate[r] * (A[r] . B[e, n] + bias[e, n])  (fp32)
-cudaError_t launch_ffn_simt(const Dims &D, int epi, const void *A, int64_t K, const void *B, const void *bias,
-                            int64_t N_out, const float *row_gate, const int32_t *offsets, void *out,
+// a_rows: rows of A that exist (rows past it read as zeros).
+cudaError_t launch_ffn_simt(const Dims &D, int epi, const void *A, int64_t a_rows, int64_t K, const void *B,
+                            const void *bias, int64_t N_out, const float *row_gate, const int32_t *offsets, void *out,
                             int32_t *status, cudaStream_t s);
 
 // tcgen05 path (bf16). Returns cudaErrorNotSupported when the shape is not
@@ -230,8 +232,12 @@ inline int64_t ffn_sync_ints(const Dims &D) {
 // Both expert GEMMs of a bf16 config in one launch on CTA pairs; blk_done
 // [ffn_blocks_max + 1] int32 counts stored h tiles per block (zero on entry,
 // left zero on exit).
-cudaError_t launch_ffn_tc(const Dims &D, const void *x_perm, const int32_t *offsets, const void *w1,
+// a_rows: rows of x_perm that exist (TMA zero-fills the rest up to R_max).
+cudaError_t launch_ffn_tc(const Dims &D, const void *x_perm, int64_t a_rows, const int32_t *offsets, const void *w1,
                           const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
                           float *y_perm, int32_t *blk_done, int32_t *status, cudaStream_t s);
+
+// The shared expert's single segment {0, Tp} and zeroed FFN counters.
+cudaError_t launch_shared_setup(int32_t *offsets, int64_t rows, int32_t *sync, int64_t n_sync, cudaStream_t s);
 
 }  // namespace moe

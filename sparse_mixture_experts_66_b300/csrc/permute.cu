@@ -81,8 +81,9 @@ template <typename T, int KM>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float *__restrict__ y_perm, int64_t d,
                                                                   const int32_t *__restrict__ row_of,
                                                                   const float *__restrict__ gate,
-                                                                  const T *__restrict__ x, int64_t T_, int k,
-                                                                  int64_t R_max, uint32_t flags,
+                                                                  const T *__restrict__ x,
+                                                                  const float *__restrict__ y_shared, int64_t T_,
+                                                                  int k, int64_t R_max, uint32_t flags,
                                                                   T *__restrict__ y, int32_t *status) {
   pdl_wait();
   constexpr int U = 8 / KM;
@@ -140,6 +141,13 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float *_
         a.w /= ksum[u];
       }
       if (ident[u]) a = Store4<T>::ld(x + (t0 + u) * d + c);
+      if (y_shared) {  // the shared expert, added last
+        const float4 sh = __ldg(reinterpret_cast<const float4 *>(y_shared + (t0 + u) * d + c));
+        a.x += sh.x;
+        a.y += sh.y;
+        a.z += sh.z;
+        a.w += sh.w;
+      }
       Store4<T>::st(y + (t0 + u) * d + c, a);
     }
   }
@@ -152,8 +160,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float *_
 template <typename T>
 __global__ void __launch_bounds__(kCombineThreads) combine_split_kernel(
     const float *__restrict__ y_perm, const float *__restrict__ y_split, int nsplit, int64_t d,
-    const int32_t *__restrict__ row_of, const float *__restrict__ gate, const T *__restrict__ x, int64_t T_, int k,
-    int64_t R_max, uint32_t flags, T *__restrict__ y, int32_t *status) {
+    const int32_t *__restrict__ row_of, const float *__restrict__ gate, const T *__restrict__ x,
+    const float *__restrict__ y_shared, int64_t T_, int k, int64_t R_max, uint32_t flags, T *__restrict__ y,
+    int32_t *status) {
   pdl_wait();
   const int64_t d4 = d >> 2;
   const int64_t i = (int64_t)blockIdx.x * kCombineThreads + threadIdx.x;
@@ -215,6 +224,13 @@ __global__ void __launch_bounds__(kCombineThreads) combine_split_kernel(
     acc.w /= kept_gate;
   }
   if ((flags & MOE_FLAG_IDENTITY_FALLBACK) && !kept) acc = Store4<T>::ld(x + t * d + c);
+  if (y_shared) {  // the shared expert, added last
+    const float4 sh = __ldg(reinterpret_cast<const float4 *>(y_shared + t * d + c));
+    acc.x += sh.x;
+    acc.y += sh.y;
+    acc.z += sh.z;
+    acc.w += sh.w;
+  }
   Store4<T>::st(y + t * d + c, acc);
 }
 
@@ -239,34 +255,50 @@ cudaError_t launch_permute(const Dims &D, const void *x, const int32_t *offsets,
 namespace {
 template <typename T>
 cudaError_t launch_combine_t(const Dims &D, const float *y_perm, const float *y_split, int nsplit,
-                             const int32_t *row_of, const float *gate, const T *x, T *y, int32_t *status,
-                             cudaStream_t s) {
+                             const int32_t *row_of, const float *gate, const T *x, const float *y_shared, T *y,
+                             int32_t *status, cudaStream_t s) {
   const int64_t items = D.T * (D.d / 4);
   if (nsplit > 0) {
     const int64_t g = (items + kCombineThreads - 1) / kCombineThreads;
     return launch_k(combine_split_kernel<T>, dim3((unsigned)g), dim3(kCombineThreads), 0, s, 1u, y_perm, y_split,
-                    nsplit, D.d, row_of, gate, x, D.T, D.k, D.R_max, D.flags, y, status);
+                    nsplit, D.d, row_of, gate, x, y_shared, D.T, D.k, D.R_max, D.flags, y, status);
   }
   const int km = D.k <= 1 ? 1 : D.k <= 2 ? 2 : D.k <= 4 ? 4 : 8;
   const int64_t tok_per_block = 8 / km;
   const unsigned g = (unsigned)((D.T + tok_per_block - 1) / tok_per_block);
   auto kern = km == 1 ? combine_kernel<T, 1> : km == 2 ? combine_kernel<T, 2> : km == 4 ? combine_kernel<T, 4>
                                                                                     : combine_kernel<T, 8>;
-  return launch_k(kern, dim3(g), dim3(kCombineThreads), 0, s, 1u, y_perm, D.d, row_of, gate, x, D.T, D.k, D.R_max,
-                  D.flags, y, status);
+  return launch_k(kern, dim3(g), dim3(kCombineThreads), 0, s, 1u, y_perm, D.d, row_of, gate, x, y_shared, D.T, D.k,
+                  D.R_max, D.flags, y, status);
 }
 }  // namespace
 
 cudaError_t launch_combine(const Dims &D, const float *y_perm, const float *y_split, int nsplit,
-                           const int32_t *row_of, const float *gate, const void *x, void *y, int32_t *status,
-                           cudaStream_t s) {
+                           const int32_t *row_of, const float *gate, const void *x, const float *y_shared, void *y,
+                           int32_t *status, cudaStream_t s) {
   if (!y_split) nsplit = 0;
   if (nsplit > 7 || D.k > 8) return cudaErrorNotSupported;
   if (D.T == 0) return cudaSuccess;
   if (D.dt == MOE_DT_BF16)
     return launch_combine_t<__nv_bfloat16>(D, y_perm, y_split, nsplit, row_of, gate, (const __nv_bfloat16 *)x,
-                                           (__nv_bfloat16 *)y, status, s);
-  return launch_combine_t<float>(D, y_perm, y_split, nsplit, row_of, gate, (const float *)x, (float *)y, status, s);
+                                           y_shared, (__nv_bfloat16 *)y, status, s);
+  return launch_combine_t<float>(D, y_perm, y_split, nsplit, row_of, gate, (const float *)x, y_shared, (float *)y,
+                                 status, s);
+}
+
+namespace {
+__global__ void shared_setup_kernel(int32_t *offsets, int64_t rows, int32_t *sync, int64_t n_sync) {
+  pdl_wait();
+  if (threadIdx.x == 0) {
+    offsets[0] = 0;
+    offsets[1] = (int32_t)rows;
+  }
+  for (int64_t i = threadIdx.x; i < n_sync; i += blockDim.x) sync[i] = 0;
+}
+}  // namespace
+
+cudaError_t launch_shared_setup(int32_t *offsets, int64_t rows, int32_t *sync, int64_t n_sync, cudaStream_t s) {
+  return launch_k(shared_setup_kernel, dim3(1), dim3(256), 0, s, 1u, offsets, rows, sync, n_sync);
 }
 
 }  // namespace moe

@@ -34,6 +34,7 @@ MOE_DT_F32 = 0
 MOE_DT_BF16 = 1
 MOE_FLAG_RENORM_SURVIVORS = 1
 MOE_FLAG_IDENTITY_FALLBACK = 2
+MOE_FLAG_SHARED_EXPERT = 4
 MOE_FLAG_ROUTER_STATS = 8
 
 _DT_CODE = {torch.float32: MOE_DT_F32, torch.bfloat16: MOE_DT_BF16}
@@ -59,7 +60,8 @@ class MoeConfig(ctypes.Structure):
 class MoeWorkspaceLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "status", "topk_idx", "gate", "score", "counts_raw", "counts_kept", "offsets", "sel_thr", "sel_eq",
-        "row_of", "row_token", "row_gate", "x_perm", "h", "y_perm", "y_split", "ffn_sync", "probs", "lse", "total")] + [
+        "row_of", "row_token", "row_gate", "x_perm", "h", "y_perm", "y_split", "ffn_sync", "probs", "lse", "shared_offsets", "h_shared", "y_shared",
+        "shared_sync", "total")] + [
         ("rows", ctypes.c_int64), ("capacity", ctypes.c_int64)]
 
 
@@ -80,6 +82,8 @@ SIGNATURES = {
     "moe_forward": (["C"] + ["P"] * 9 + ["S"], ctypes.c_int),
     "moe_forward_noalloc": (["C"] + ["P"] * 8 + ["S"], ctypes.c_int),
     "moe_router_stats": (["C"] + ["P"] * 5 + ["S"], ctypes.c_int),
+    "moe_shared_expert": (["C"] + ["P"] * 6 + ["S"], ctypes.c_int),
+    "moe_forward_shared": (["C"] + ["P"] * 13 + ["S"], ctypes.c_int),
 }
 _KIND = {"C": ctypes.POINTER(MoeConfig), "P": ctypes.c_void_p, "S": ctypes.c_void_p,
          "L": ctypes.POINTER(MoeWorkspaceLayout)}
@@ -204,6 +208,17 @@ def moe_forward(cfg, x, w_g, router_bias, w1, b1, w2, b2, y, ws, stream=None):
                               _ptr(w2), _ptr(b2), _ptr(y), _ptr(ws), _stream(stream)))
 
 
+def moe_shared_expert(cfg, x, sw1, sb1, sw2, sb2, ws, stream=None):
+    _check(load().moe_shared_expert(ctypes.byref(cfg), _ptr(x), _ptr(sw1), _ptr(sb1), _ptr(sw2), _ptr(sb2), _ptr(ws),
+                                    _stream(stream)))
+
+
+def moe_forward_shared(cfg, x, w_g, router_bias, w1, b1, w2, b2, sw1, sb1, sw2, sb2, y, ws, stream=None):
+    _check(load().moe_forward_shared(ctypes.byref(cfg), _ptr(x), _ptr(w_g), _ptr(router_bias), _ptr(w1), _ptr(b1),
+                                     _ptr(w2), _ptr(b2), _ptr(sw1), _ptr(sb1), _ptr(sw2), _ptr(sb2), _ptr(y),
+                                     _ptr(ws), _stream(stream)))
+
+
 def moe_forward_noalloc(cfg, x, w_g, router_bias, w1, b1, w2, b2, y, stream=None):
     """moe_forward without a workspace, for callers that cannot allocate device
     memory: the library's fixed 32 MiB device scratch array is used instead.
@@ -245,7 +260,9 @@ class Workspace:
             y_perm=self.view("y_perm", torch.float32, (R, c.d)),
             y_split=self.view("y_split", torch.float32, (self.splits - 1, R, c.d)),
             probs=self.view("probs", torch.float32, (T, N) if c.flags & MOE_FLAG_ROUTER_STATS else (0, N)),
-            lse=self.view("lse", torch.float32, (T,) if c.flags & MOE_FLAG_ROUTER_STATS else (0,)))
+            lse=self.view("lse", torch.float32, (T,) if c.flags & MOE_FLAG_ROUTER_STATS else (0,)),
+            y_shared=self.view("y_shared", torch.float32,
+                               ((T + 127) // 128 * 128, c.d) if c.flags & MOE_FLAG_SHARED_EXPERT else (0, c.d)))
 
     @property
     def splits(self):

@@ -119,6 +119,21 @@ def draw(w: Workload, draw_x: bool = True) -> dict:
     return out
 
 
+def draw_shared(w: Workload, seed: int = 1) -> dict:
+    """Weights of a shared (always-on) expert with the routed experts' shapes
+    and laws: sw1 [d_ff, d], sb1 [d_ff], sw2 [d, d_ff], sb2 [d], from their own
+    seeded generator (drawn in that order)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    dt = DTYPES[w.dtype]
+
+    def normal(shape, std):
+        return (torch.randn(*shape, generator=g, dtype=torch.float32) * std).to(dt)
+
+    return {"sw1": normal((w.d_ff, w.d), 1.0 / math.sqrt(w.d)), "sb1": normal((w.d_ff,), 0.1),
+            "sw2": normal((w.d, w.d_ff), 1.0 / math.sqrt(w.d_ff)), "sb2": normal((w.d,), 0.1)}
+
+
 def draw_x_only(w: Workload, seed: int) -> torch.Tensor:
     """A fresh token batch of the workload's shape from another seed."""
     g = torch.Generator(device="cpu")

@@ -72,7 +72,7 @@ def test_workspace_layout_is_aligned_and_sized():
         L = moe.moe_get_workspace_layout(cfg)
         S = min(w.T * w.k, w.N * L.capacity)
         assert L.rows == (S + 127 * w.N) // 128 * 128
-        offs = [getattr(L, f) for f, _ in moe.MoeWorkspaceLayout._fields_[:19]]
+        offs = [getattr(L, f) for f, _ in moe.MoeWorkspaceLayout._fields_[:23]]
         assert all(o % 256 == 0 for o in offs)
         assert offs == sorted(offs)
         es = 2 if w.dtype == "bf16" else 4
@@ -148,3 +148,19 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros(8, 8)
     with pytest.raises(ValueError, match="CUDA"):
         moe.moe_forward(cfg, x, x, None, x, x, x, x, x, x, stream=None)
+
+
+def test_shared_expert_entry_points_check_their_flag():
+    lib = moe.load()
+    p = ctypes.c_void_p(0x1000)
+    cfg = moe.make_config(64, 64, 64, 8, 2, 1.25)
+    st = lib.moe_shared_expert(ctypes.byref(cfg), p, p, p, p, p, p, None)
+    assert st == moe.MOE_ERR_INVALID_ARG and b"MOE_FLAG_SHARED_EXPERT" in lib.moe_last_error()
+    st = lib.moe_forward_shared(ctypes.byref(cfg), *([p] * 13), None)
+    assert st == moe.MOE_ERR_INVALID_ARG and b"MOE_FLAG_SHARED_EXPERT" in lib.moe_last_error()
+    cfg.flags = moe.MOE_FLAG_SHARED_EXPERT
+    # moe_forward has no shared weights to run it with
+    st = lib.moe_forward(ctypes.byref(cfg), p, p, None, p, p, p, p, p, p, None)
+    assert st == moe.MOE_ERR_INVALID_ARG and b"moe_forward_shared" in lib.moe_last_error()
+    L = moe.moe_get_workspace_layout(cfg)
+    assert L.y_shared - L.h_shared >= 128 * 64 * 2 and L.shared_sync - L.y_shared >= 128 * 64 * 4

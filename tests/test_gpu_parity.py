@@ -300,3 +300,66 @@ def test_router_stats_leave_routing_unchanged():
     for key in ("topk_idx", "gate", "score", "row_of", "offsets"):
         assert np.array_equal(a[key], b[key]), key
     assert torch.equal(a["_y"], b["_y"])
+
+
+# ---------------------------------------------------------------------------
+# Shared always-on expert (MOE_FLAG_SHARED_EXPERT)
+# ---------------------------------------------------------------------------
+SHARED_CASES = [
+    custom(1000, 256, 1408, 8, 2, 1.25, seed=1),  # bf16, CTA-pair routed FFN
+    custom(300, 256, 512, 8, 2, 1.25, router_bias="zipf", seed=30),  # T not a multiple of 128, drops
+    custom(48, 512, 2048, 8, 2, 1.0, router_bias="zipf", seed=14),  # decode-shaped routed FFN
+    WORKLOADS[SMALL_FP32],  # fp32 SIMT path
+]
+
+
+@pytest.mark.parametrize("w", SHARED_CASES, ids=lambda w: w.name)
+def test_shared_expert_against_oracle(w):
+    """moe_forward_shared equals the oracle's forward with the shared expert
+    added to every token, under the same parity rules as the routed layer."""
+    from sparse_mixture_experts_66_b300.workload import draw_shared
+    inp = draw(w)
+    sh = draw_shared(w)
+    cfg = moe.config_of(w, moe.MOE_FLAG_SHARED_EXPERT)
+    dev = parity.to_device(inp)
+    shd = {k: v.cuda() for k, v in sh.items()}
+    ws = moe.Workspace(cfg)
+    y = torch.empty_like(dev["x"])
+    moe.moe_forward_shared(cfg, dev["x"], dev["w_g"], dev["router_bias"], dev["w1"], dev["b1"], dev["w2"], dev["b2"],
+                           shd["sw1"], shd["sb1"], shd["sw2"], shd["sb2"], y, ws.buf)
+    ws.status()
+    v = ws.views()
+    g = {k: t.cpu().numpy() for k, t in v.items() if k not in ("x_perm", "h", "y_perm", "y_split", "y_shared")}
+    g["y"] = y.float().cpu().numpy().astype(np.float64)
+    ref = O.load().forward(*(as_f32_numpy(inp[n]) for n in ("x", "w_g", "w1", "b1", "w2", "b2")), k=w.k,
+                           cf=w.capacity_factor, router_bias=as_f32_numpy(inp["router_bias"]),
+                           shared=tuple(as_f32_numpy(sh[n]) for n in ("sw1", "sb1", "sw2", "sb2")))
+    rep = parity.compare(w, g, ref)
+    print(w.name, rep)
+
+
+def test_shared_expert_stage_call_composes():
+    """moe_shared_expert + moe_combine on the stage calls give moe_forward_shared's output bit for bit."""
+    from sparse_mixture_experts_66_b300.workload import draw_shared
+    w = SHARED_CASES[1]
+    inp, sh = draw(w), draw_shared(w)
+    cfg = moe.config_of(w, moe.MOE_FLAG_SHARED_EXPERT)
+    d = parity.to_device(inp)
+    s = {k: t.cuda() for k, t in sh.items()}
+    ws = moe.Workspace(cfg)
+    y1 = torch.empty_like(d["x"])
+    moe.moe_forward_shared(cfg, d["x"], d["w_g"], d["router_bias"], d["w1"], d["b1"], d["w2"], d["b2"], s["sw1"],
+                           s["sb1"], s["sw2"], s["sb2"], y1, ws.buf)
+    ws2 = moe.Workspace(cfg)
+    v = ws2.views()
+    moe.moe_route(cfg, d["x"], d["w_g"], d["router_bias"], v["topk_idx"], v["gate"], v["score"], ws2.buf)
+    moe.moe_dispatch(cfg, d["x"], v["topk_idx"], v["gate"], v["score"], v["counts_raw"], v["counts_kept"],
+                     v["offsets"], v["row_of"], v["row_token"], v["row_gate"], v["x_perm"], ws2.buf)
+    moe.moe_expert_ffn(cfg, v["x_perm"], v["offsets"], d["w1"], d["b1"], d["w2"], d["b2"], v["row_gate"], v["h"],
+                       v["y_perm"], ws2.buf)
+    moe.moe_shared_expert(cfg, d["x"], s["sw1"], s["sb1"], s["sw2"], s["sb2"], ws2.buf)
+    y2 = torch.empty_like(d["x"])
+    moe.moe_combine(cfg, v["y_perm"], v["row_of"], v["gate"], d["x"], y2, ws2.buf)
+    ws.status()
+    ws2.status()
+    assert torch.equal(y1, y2)
