@@ -86,7 +86,18 @@ enum {
   /* The router also stores every token's full probability row and the
    * logsumexp of its logits in the workspace (probs, lse), for
    * moe_router_stats. Routing results are unchanged. */
-  MOE_FLAG_ROUTER_STATS = 8u
+  MOE_FLAG_ROUTER_STATS = 8u,
+  /* Expert-choice routing ("Mixture of Experts (MoE): Architecture, Routing,
+   * and Scaling" and "Mixture of Experts: Scaling Language Models with Sparse
+   * Activation", "Expert Choice Routing"): instead of each token picking k
+   * experts, each expert takes the C tokens with the highest probability
+   * p[t, e] (equal probabilities: lower token first; C from cfg's k and
+   * capacity_factor as usual), and a token's output is the sum, in expert
+   * order, of p[t, e] * E_e(x_t) over the experts that took it (0 if none).
+   * Only moe_forward runs it (with MOE_FLAG_ROUTER_STATS at most); the
+   * workspace's row_of is then [T, N] (the row of token t at expert e, or
+   * -1) and probs holds p. */
+  MOE_FLAG_EXPERT_CHOICE = 16u
 };
 
 typedef struct {

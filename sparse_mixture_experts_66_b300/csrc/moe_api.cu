@@ -51,16 +51,22 @@ moe_status check_config(const moe_config *cfg, Dims *D) {
     return fail(MOE_ERR_INVALID_ARG, "d and d_ff must be >= 8 and multiples of %lld (got d=%lld d_ff=%lld)",
                 (long long)mult, (long long)cfg->d, (long long)cfg->d_ff);
   if (cfg->flags & ~(uint32_t)(MOE_FLAG_RENORM_SURVIVORS | MOE_FLAG_IDENTITY_FALLBACK | MOE_FLAG_ROUTER_STATS |
-                               MOE_FLAG_SHARED_EXPERT))
+                               MOE_FLAG_SHARED_EXPERT | MOE_FLAG_EXPERT_CHOICE))
     return fail(MOE_ERR_INVALID_ARG, "unknown flag bits 0x%x", cfg->flags);
+  const bool ec = (cfg->flags & MOE_FLAG_EXPERT_CHOICE) != 0;
+  if (ec && (cfg->flags & ~(uint32_t)(MOE_FLAG_EXPERT_CHOICE | MOE_FLAG_ROUTER_STATS)))
+    return fail(MOE_ERR_INVALID_ARG, "MOE_FLAG_EXPERT_CHOICE combines only with MOE_FLAG_ROUTER_STATS");
+  if (ec && cfg->T * (int64_t)cfg->N >= ((int64_t)1 << 31)) return fail(MOE_ERR_INVALID_ARG, "T*N must be < 2^31");
   if (isnan(cfg->capacity_factor)) return fail(MOE_ERR_INVALID_ARG, "capacity_factor is NaN");
   D->T = cfg->T;
   D->d = cfg->d;
   D->d_ff = cfg->d_ff;
   D->N = cfg->N;
-  D->k = cfg->k;
   D->C = capacity_of(cfg->T, cfg->N, cfg->k, cfg->capacity_factor);
-  int64_t S = cfg->T * (int64_t)cfg->k;
+  // expert choice: every token offers itself to every expert, so the
+  // selection, dispatch and combine run with k = N requests per token
+  D->k = ec ? cfg->N : cfg->k;
+  int64_t S = cfg->T * (int64_t)D->k;
   if ((int64_t)cfg->N * D->C < S) S = (int64_t)cfg->N * D->C;
   D->R_max = (S + (int64_t)(kRowAlign - 1) * cfg->N) / kRowAlign * kRowAlign;
   if (D->R_max >= ((int64_t)1 << 31)) return fail(MOE_ERR_INVALID_ARG, "too many permuted rows");
@@ -107,7 +113,7 @@ void make_layout(const Dims &D, moe_workspace_layout *L) {
   const int S = decode_splits(D);
   L->y_split = take(S > 1 ? (size_t)(S - 1) * R * (size_t)D.d * 4 : 0);
   L->ffn_sync = take((size_t)ffn_sync_ints(D) * 4);
-  const bool stats = (D.flags & MOE_FLAG_ROUTER_STATS) != 0;
+  const bool stats = (D.flags & (MOE_FLAG_ROUTER_STATS | MOE_FLAG_EXPERT_CHOICE)) != 0;
   L->probs = take(stats ? (size_t)D.T * N * 4 : 0);
   L->lse = take(stats ? (size_t)D.T * 4 : 0);
   const bool shared = (D.flags & MOE_FLAG_SHARED_EXPERT) != 0;
@@ -145,14 +151,18 @@ moe_status check_opt(const void *p, const char *what) {
 moe_status do_route(const Dims &D, const moe_workspace_layout &L, const void *x, const void *w_g,
                     const float *router_bias, int32_t *topk_idx, float *gate, float *score, void *ws,
                     cudaStream_t s) {
-  // with MOE_FLAG_ROUTER_STATS the router also stores full probability rows and logsumexps
-  const bool stats = (D.flags & MOE_FLAG_ROUTER_STATS) != 0;
+  // with MOE_FLAG_ROUTER_STATS (or expert choice) the router also stores full
+  // probability rows and logsumexps
+  const bool ec = (D.flags & MOE_FLAG_EXPERT_CHOICE) != 0;
+  const bool stats = ec || (D.flags & MOE_FLAG_ROUTER_STATS) != 0;
   float *probs = stats ? AT(ws, L.probs, float *) : nullptr;
   float *lse = stats ? AT(ws, L.lse, float *) : nullptr;
-  cudaError_t e = D.dt == MOE_DT_BF16 && !router_split(D)
-                      ? launch_router_tc(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse,
+  Dims Dr = D;
+  if (ec) Dr.k = 1;  // expert choice uses the probabilities; the top-1 pick is not read
+  cudaError_t e = D.dt == MOE_DT_BF16 && !router_split(Dr)
+                      ? launch_router_tc(Dr, x, w_g, router_bias, topk_idx, gate, score, probs, lse,
                                          AT(ws, L.status, int32_t *), s)
-                      : launch_router(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse,
+                      : launch_router(Dr, x, w_g, router_bias, topk_idx, gate, score, probs, lse,
                                       AT(ws, L.status, int32_t *), s);
   if (e != cudaSuccess) return cuda_fail(e, "router launch");
   return MOE_OK;
@@ -294,6 +304,8 @@ moe_status moe_route(const moe_config *cfg, const void *x, const void *w_g, cons
                      int32_t *topk_idx, float *gate, float *score, void *ws, moe_stream_t stream) {
   Dims D;
   TRY(check_config(cfg, &D));
+  if (D.flags & MOE_FLAG_EXPERT_CHOICE)
+    return fail(MOE_ERR_INVALID_ARG, "moe_route: expert-choice routing runs only through moe_forward");
   TRY(check_ptrs({x, w_g, topk_idx, gate, score, ws}, "moe_route"));
   TRY(check_opt(router_bias, "moe_route router_bias"));
   moe_workspace_layout L;
@@ -322,6 +334,8 @@ moe_status moe_dispatch(const moe_config *cfg, const void *x, const int32_t *top
                         moe_stream_t stream) {
   Dims D;
   TRY(check_config(cfg, &D));
+  if (D.flags & MOE_FLAG_EXPERT_CHOICE)
+    return fail(MOE_ERR_INVALID_ARG, "moe_dispatch: expert-choice routing runs only through moe_forward");
   TRY(check_ptrs({x, topk_idx, gate, score, counts_raw, counts_kept, offsets, row_of, row_token, row_gate, x_perm,
                   ws},
                  "moe_dispatch"));
@@ -336,6 +350,8 @@ moe_status moe_expert_ffn(const moe_config *cfg, const void *x_perm, const int32
                           float *y_perm, void *ws, moe_stream_t stream) {
   Dims D;
   TRY(check_config(cfg, &D));
+  if (D.flags & MOE_FLAG_EXPERT_CHOICE)
+    return fail(MOE_ERR_INVALID_ARG, "moe_expert_ffn: expert-choice routing runs only through moe_forward");
   TRY(check_ptrs({x_perm, offsets, w1, b1, w2, b2, y_perm, ws}, "moe_expert_ffn"));
   TRY(check_opt(row_gate, "moe_expert_ffn row_gate"));
   TRY(check_opt(h, "moe_expert_ffn h"));
@@ -349,6 +365,8 @@ moe_status moe_combine(const moe_config *cfg, const float *y_perm, const int32_t
                        const void *x, void *y, void *ws, moe_stream_t stream) {
   Dims D;
   TRY(check_config(cfg, &D));
+  if (D.flags & MOE_FLAG_EXPERT_CHOICE)
+    return fail(MOE_ERR_INVALID_ARG, "moe_combine: expert-choice routing runs only through moe_forward");
   TRY(check_ptrs({y_perm, row_of, y, ws}, "moe_combine"));
   if ((D.flags & MOE_FLAG_RENORM_SURVIVORS)) TRY(check_ptrs({gate}, "moe_combine gate (renormalise flag)"));
   if ((D.flags & MOE_FLAG_IDENTITY_FALLBACK)) TRY(check_ptrs({x}, "moe_combine x (identity fallback flag)"));
@@ -391,6 +409,14 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const void *w_g, co
   void *x_perm = AT(ws, L.x_perm, void *);
   float *y_perm = AT(ws, L.y_perm, float *);
   TRY(do_route(D, L, x, w_g, router_bias, topk_idx, gate, score, ws, s));
+  if (D.flags & MOE_FLAG_EXPERT_CHOICE) {
+    // every token offers itself to every expert (request j of token t goes to
+    // expert j), ranked and weighted by p[t, j]: the capacity step then keeps
+    // each expert's C most probable tokens
+    cudaError_t e = launch_ec_pattern(topk_idx, D.T, D.N, s);
+    if (e != cudaSuccess) return cuda_fail(e, "expert-choice request pattern");
+    gate = score = AT(ws, L.probs, float *);
+  }
   TRY(do_dispatch(D, L, x, topk_idx, gate, score, AT(ws, L.counts_raw, int32_t *), AT(ws, L.counts_kept, int32_t *),
                   offsets, row_of, AT(ws, L.row_token, int32_t *), row_gate, x_perm, ws, s));
   TRY(do_ffn(D, L, x_perm, offsets, w1, b1, w2, b2, row_gate, AT(ws, L.h, void *), y_perm, ws, s));

@@ -237,6 +237,9 @@ cudaError_t launch_ffn_tc(const Dims &D, const void *x_perm, int64_t a_rows, con
                           const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
                           float *y_perm, int32_t *blk_done, int32_t *status, cudaStream_t s);
 
+// Expert-choice requests: idx[t * N + j] = j for every token.
+cudaError_t launch_ec_pattern(int32_t *idx, int64_t T, int N, cudaStream_t s);
+
 // The shared expert's single segment {0, Tp} and zeroed FFN counters.
 cudaError_t launch_shared_setup(int32_t *offsets, int64_t rows, int32_t *sync, int64_t n_sync, cudaStream_t s);
 

@@ -153,6 +153,43 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float *_
   }
 }
 
+// Combine of many picks per token (k > 8: expert-choice routing, where every
+// expert may take a token): a CTA owns one token, threads stride its columns;
+// the picks are walked in order and most are -1. No flag variants apply.
+__global__ void __launch_bounds__(kCombineThreads) combine_many_kernel(const float *__restrict__ y_perm, int64_t d,
+                                                                       const int32_t *__restrict__ row_of, int k,
+                                                                       int64_t R_max, int64_t T_, void *y_out,
+                                                                       int bf16, int32_t *status) {
+  pdl_wait();
+  const int64_t t = blockIdx.x;
+  if (t >= T_) return;
+  for (int64_t c = (int64_t)threadIdx.x * 4; c < d; c += kCombineThreads * 4) {
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+      const int32_t r = __ldg(row_of + t * k + j);
+      if (r < 0) continue;
+      if (r >= R_max) {
+        if (c == 0) report_error(status, MOE_ERR_BOUNDS, kKCombine, (int32_t)t);
+        continue;
+      }
+      const float4 v = __ldg(reinterpret_cast<const float4 *>(y_perm + (int64_t)r * d + c));
+      a.x += v.x;
+      a.y += v.y;
+      a.z += v.z;
+      a.w += v.w;
+    }
+    if (bf16) Store4<__nv_bfloat16>::st(reinterpret_cast<__nv_bfloat16 *>(y_out) + t * d + c, a);
+    else Store4<float>::st(reinterpret_cast<float *>(y_out) + t * d + c, a);
+  }
+}
+
+__global__ void ec_pattern_kernel(int32_t *idx, int64_t T_, int N) {
+  pdl_wait();
+  const int64_t n = T_ * N;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    idx[i] = (int32_t)(i % N);
+}
+
 // Combine with the K slices of a decode-mode second GEMM: one thread per
 // (token, 4 columns); the k x (1 + nsplit) source rows are walked as one flat
 // list, 8 loads at a time. Per pick the slices are added in slice order, then
@@ -170,28 +207,31 @@ __global__ void __launch_bounds__(kCombineThreads) combine_split_kernel(
   const int64_t t = i / d4;
   const int64_t c = (i - t * d4) << 2;
   const int per = 1 + nsplit, nsrc = k * per;
-  uint32_t kept = 0;  // bit j: pick j kept
+  int nkept = 0;
   float kept_gate = 0.f;
   for (int j = 0; j < k; ++j) {
     const int32_t r = __ldg(row_of + t * k + j);
     if (r >= R_max && c == 0) report_error(status, MOE_ERR_BOUNDS, kKCombine, (int32_t)t);
     if (r >= 0 && r < R_max) {
-      kept |= 1u << j;
+      ++nkept;
       if (flags & MOE_FLAG_RENORM_SURVIVORS) kept_gate += __ldg(gate + t * k + j);
     }
   }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), part = acc;
   for (int q0 = 0; q0 < nsrc; q0 += 8) {
     float4 v[8];
+    bool ok[8];  // the source's pick is kept
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
       const int q = q0 + b;
       const int j = q / per, sl = q - j * per;
       const float *src = y_perm;
       int64_t r = 0;
+      ok[b] = false;
       if (q < nsrc) {
         const int32_t rr = __ldg(row_of + t * k + j);
-        r = (rr >= 0 && rr < R_max) ? rr : 0;
+        ok[b] = rr >= 0 && rr < R_max;
+        r = ok[b] ? rr : 0;
         if (sl > 0) src = y_split + (int64_t)(sl - 1) * R_max * d;
       }
       v[b] = __ldg(reinterpret_cast<const float4 *>(src + r * d + c));
@@ -206,7 +246,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_split_kernel(
         part.z += v[b].z;
         part.w += v[b].w;
         if (sl == nsplit) {
-          if (kept & (1u << j)) {
+          if (ok[b]) {
             acc.x += part.x;
             acc.y += part.y;
             acc.z += part.z;
@@ -217,13 +257,13 @@ __global__ void __launch_bounds__(kCombineThreads) combine_split_kernel(
       }
     }
   }
-  if ((flags & MOE_FLAG_RENORM_SURVIVORS) && kept) {
+  if ((flags & MOE_FLAG_RENORM_SURVIVORS) && nkept > 0) {
     acc.x /= kept_gate;
     acc.y /= kept_gate;
     acc.z /= kept_gate;
     acc.w /= kept_gate;
   }
-  if ((flags & MOE_FLAG_IDENTITY_FALLBACK) && !kept) acc = Store4<T>::ld(x + t * d + c);
+  if ((flags & MOE_FLAG_IDENTITY_FALLBACK) && nkept == 0) acc = Store4<T>::ld(x + t * d + c);
   if (y_shared) {  // the shared expert, added last
     const float4 sh = __ldg(reinterpret_cast<const float4 *>(y_shared + t * d + c));
     acc.x += sh.x;
@@ -277,8 +317,13 @@ cudaError_t launch_combine(const Dims &D, const float *y_perm, const float *y_sp
                            const int32_t *row_of, const float *gate, const void *x, const float *y_shared, void *y,
                            int32_t *status, cudaStream_t s) {
   if (!y_split) nsplit = 0;
-  if (nsplit > 7 || D.k > 8) return cudaErrorNotSupported;
+  if (nsplit > 7) return cudaErrorNotSupported;
   if (D.T == 0) return cudaSuccess;
+  if (D.k > 8 && nsplit == 0) {
+    if (y_shared || (D.flags & (MOE_FLAG_RENORM_SURVIVORS | MOE_FLAG_IDENTITY_FALLBACK))) return cudaErrorNotSupported;
+    return launch_k(combine_many_kernel, dim3((unsigned)D.T), dim3(kCombineThreads), 0, s, 1u, y_perm, D.d, row_of,
+                    D.k, D.R_max, D.T, y, D.dt == MOE_DT_BF16 ? 1 : 0, status);
+  }
   if (D.dt == MOE_DT_BF16)
     return launch_combine_t<__nv_bfloat16>(D, y_perm, y_split, nsplit, row_of, gate, (const __nv_bfloat16 *)x,
                                            y_shared, (__nv_bfloat16 *)y, status, s);
@@ -296,6 +341,12 @@ __global__ void shared_setup_kernel(int32_t *offsets, int64_t rows, int32_t *syn
   for (int64_t i = threadIdx.x; i < n_sync; i += blockDim.x) sync[i] = 0;
 }
 }  // namespace
+
+cudaError_t launch_ec_pattern(int32_t *idx, int64_t T, int N, cudaStream_t s) {
+  int64_t g = (T * N + 255) / 256;
+  if (g > 148 * 16) g = 148 * 16;
+  return launch_k(ec_pattern_kernel, dim3((unsigned)g), dim3(256), 0, s, 1u, idx, T, N);
+}
 
 cudaError_t launch_shared_setup(int32_t *offsets, int64_t rows, int32_t *sync, int64_t n_sync, cudaStream_t s) {
   return launch_k(shared_setup_kernel, dim3(1), dim3(256), 0, s, 1u, offsets, rows, sync, n_sync);

@@ -36,6 +36,7 @@ MOE_FLAG_RENORM_SURVIVORS = 1
 MOE_FLAG_IDENTITY_FALLBACK = 2
 MOE_FLAG_SHARED_EXPERT = 4
 MOE_FLAG_ROUTER_STATS = 8
+MOE_FLAG_EXPERT_CHOICE = 16
 
 _DT_CODE = {torch.float32: MOE_DT_F32, torch.bfloat16: MOE_DT_BF16}
 _DT_TORCH = {MOE_DT_F32: torch.float32, MOE_DT_BF16: torch.bfloat16}
@@ -249,6 +250,8 @@ class Workspace:
     def views(self):
         c, L = self.cfg, self.layout
         T, k, N, R = c.T, c.k, c.N, L.rows
+        if c.flags & MOE_FLAG_EXPERT_CHOICE:
+            k = N  # every token offers itself to every expert
         dt = c.torch_dtype
         return dict(
             topk_idx=self.view("topk_idx", torch.int32, (T, k)), gate=self.view("gate", torch.float32, (T, k)),
@@ -259,8 +262,10 @@ class Workspace:
             x_perm=self.view("x_perm", dt, (R, c.d)), h=self.view("h", dt, (R, c.d_ff)),
             y_perm=self.view("y_perm", torch.float32, (R, c.d)),
             y_split=self.view("y_split", torch.float32, (self.splits - 1, R, c.d)),
-            probs=self.view("probs", torch.float32, (T, N) if c.flags & MOE_FLAG_ROUTER_STATS else (0, N)),
-            lse=self.view("lse", torch.float32, (T,) if c.flags & MOE_FLAG_ROUTER_STATS else (0,)),
+            probs=self.view("probs", torch.float32,
+                            (T, N) if c.flags & (MOE_FLAG_ROUTER_STATS | MOE_FLAG_EXPERT_CHOICE) else (0, N)),
+            lse=self.view("lse", torch.float32,
+                          (T,) if c.flags & (MOE_FLAG_ROUTER_STATS | MOE_FLAG_EXPERT_CHOICE) else (0,)),
             y_shared=self.view("y_shared", torch.float32,
                                ((T + 127) // 128 * 128, c.d) if c.flags & MOE_FLAG_SHARED_EXPERT else (0, c.d)))
 

@@ -82,7 +82,7 @@ def test_workspace_layout_is_aligned_and_sized():
 
 
 @pytest.mark.parametrize("field,value", [("T", 0), ("N", 0), ("N", 257), ("k", 0), ("k", 9), ("d", 12),
-                                         ("d_ff", 4), ("dtype", 7), ("flags", 16)])
+                                         ("d_ff", 4), ("dtype", 7), ("flags", 32)])
 def test_invalid_config_rejected_on_host(field, value):
     cfg = moe.make_config(64, 64, 64, 8, 2, 1.25)
     setattr(cfg, field, value)
@@ -164,3 +164,19 @@ def test_shared_expert_entry_points_check_their_flag():
     assert st == moe.MOE_ERR_INVALID_ARG and b"moe_forward_shared" in lib.moe_last_error()
     L = moe.moe_get_workspace_layout(cfg)
     assert L.y_shared - L.h_shared >= 128 * 64 * 2 and L.shared_sync - L.y_shared >= 128 * 64 * 4
+
+
+def test_expert_choice_flag_rules():
+    lib = moe.load()
+    p = ctypes.c_void_p(0x1000)
+    cfg = moe.make_config(64, 64, 64, 8, 2, 1.25, flags=moe.MOE_FLAG_EXPERT_CHOICE | moe.MOE_FLAG_RENORM_SURVIVORS)
+    assert lib.moe_capacity(ctypes.byref(cfg)) == -1  # expert choice combines only with the statistics flag
+    cfg.flags = moe.MOE_FLAG_EXPERT_CHOICE
+    # the stage calls do not run expert choice
+    st = lib.moe_route(ctypes.byref(cfg), p, p, None, p, p, p, p, None)
+    assert st == moe.MOE_ERR_INVALID_ARG and b"expert-choice" in lib.moe_last_error()
+    # every token offers itself to every expert: the row maps are [T, N]
+    L = moe.moe_get_workspace_layout(cfg)
+    assert L.row_token - L.row_of >= 64 * 8 * 4
+    C = moe.moe_capacity(cfg)
+    assert C == 20 and L.rows >= 8 * 128  # C = ceil(1.25 * 64 * 2 / 8)

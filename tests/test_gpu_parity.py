@@ -363,3 +363,48 @@ def test_shared_expert_stage_call_composes():
     ws.status()
     ws2.status()
     assert torch.equal(y1, y2)
+
+
+# ---------------------------------------------------------------------------
+# Expert-choice routing (MOE_FLAG_EXPERT_CHOICE)
+# ---------------------------------------------------------------------------
+EC_CASES = [
+    custom(1000, 256, 512, 8, 2, 1.0, seed=41),  # bf16, CTA-pair FFN, k = N = 8 combine
+    custom(800, 128, 256, 16, 2, 1.0, router_bias="zipf", seed=42),  # N = 16 > 8: the many-pick combine
+    custom(40, 512, 1024, 8, 2, 1.0, seed=43),  # T <= 64: decode-shaped (swap-AB) FFN
+    custom(256, 64, 256, 4, 1, 1.25, dtype="f32", seed=44),  # fp32 SIMT path
+]
+
+
+@pytest.mark.parametrize("w", EC_CASES, ids=lambda w: w.name)
+def test_expert_choice_against_oracle(w):
+    """Each expert takes its C most probable tokens (ties: lower token); a
+    token's output sums p[t,e] E_e(x_t) over the experts that took it. Taken
+    sets must equal the oracle's at every expert whose C-th and (C+1)-th fp64
+    probabilities are not a near tie; outputs are compared on the tokens whose
+    taken sets agree."""
+    inp = draw(w)
+    g = parity.run_gpu(w, inp, flags=moe.MOE_FLAG_EXPERT_CHOICE)
+    C = O.load().capacity(w.T, w.N, w.k, w.capacity_factor)
+    ref = parity.oracle_ref(w, inp, sel=np.array([0]))
+    probs = ref["probs"]
+    taken_ref, counts_ref, y_ref = O.load().expert_choice(
+        as_f32_numpy(inp["x"]), probs, *(as_f32_numpy(inp[n]) for n in ("w1", "b1", "w2", "b2")), C)
+    taken = (g["row_of"].reshape(w.T, w.N) >= 0).astype(np.int32)
+    ties = set()
+    for e in range(w.N):
+        col = np.sort(probs[:, e])[::-1]
+        if C < w.T and col[C - 1] - col[C] <= parity.NEAR_TIE * col[C - 1]:
+            ties.add(e)
+    ok_e = np.array([e not in ties for e in range(w.N)])
+    assert np.array_equal(taken[:, ok_e], taken_ref[:, ok_e]), "taken sets differ"
+    assert np.array_equal(g["counts_kept"], np.minimum(C, w.T) * np.ones(w.N, dtype=np.int32))
+    tok_ok = np.all(taken == taken_ref, axis=1)
+    assert tok_ok.sum() >= 0.99 * w.T
+    # the GPU's weights are its fp32 probabilities: rows carry p[t, e]
+    rows = g["row_of"].reshape(w.T, w.N)
+    tt, ee = np.nonzero(rows >= 0)
+    assert np.allclose(g["row_gate"][rows[tt, ee]], probs[tt, ee], rtol=2e-5, atol=1e-7)
+    scale = np.max(np.abs(y_ref[tok_ok]))
+    err = np.max(np.abs(g["y"][tok_ok] - y_ref[tok_ok]))
+    assert err <= parity.TOL[w.dtype] * scale, (err, scale)
