@@ -15,7 +15,9 @@ namespace {
 
 constexpr int BM = 64, BN = 64, BK = 16;
 
-template <typename Tin, typename Tout, int EPI>
+// kRowBound: A has fewer rows than the segments cover (the shared expert reads
+// x in place); rows past a_rows read as zeros.
+template <typename Tin, typename Tout, int EPI, bool kRowBound>
 __global__ void __launch_bounds__(256) ffn_simt_kernel(const Tin *__restrict__ A, int64_t a_rows, int64_t K,
                                                        const Tin *__restrict__ B, const Tin *__restrict__ bias,
                                                        int64_t N_out, const float *__restrict__ row_gate,
@@ -42,7 +44,7 @@ __global__ void __launch_bounds__(256) ffn_simt_kernel(const Tin *__restrict__ A
       const int l = tid + q * 256;
       const int r = l / BK, c = l % BK;
       const int64_t kk = k0 + c;
-      As[c][r] = (kk < K && m0 + r < a_rows) ? to_f32(A[(m0 + r) * K + kk]) : 0.f;
+      As[c][r] = (kk < K && (!kRowBound || m0 + r < a_rows)) ? to_f32(A[(m0 + r) * K + kk]) : 0.f;
       const int64_t n = n0 + r;
       Bs[c][r] = (kk < K && n < N_out) ? to_f32(Be[n * K + kk]) : 0.f;
     }
@@ -85,17 +87,21 @@ cudaError_t launch_ffn_simt(const Dims &D, int epi, const void *A, int64_t a_row
                             int32_t *status, cudaStream_t s) {
   (void)status;
   const dim3 grid((unsigned)((N_out + BN - 1) / BN), (unsigned)(D.R_max / BM));
-  if (D.dt == MOE_DT_F32)
-    return launch_k(epi == 1 ? ffn_simt_kernel<float, float, 1> : ffn_simt_kernel<float, float, 2>, grid, dim3(256),
-                    0, s, 1u, (const float *)A, a_rows, K, (const float *)B, (const float *)bias, N_out, row_gate, offsets,
-                    D.N, (float *)out);
+  const bool bound = a_rows < D.R_max;
+  if (D.dt == MOE_DT_F32) {
+    auto kern = epi == 1 ? (bound ? ffn_simt_kernel<float, float, 1, true> : ffn_simt_kernel<float, float, 1, false>)
+                         : (bound ? ffn_simt_kernel<float, float, 2, true> : ffn_simt_kernel<float, float, 2, false>);
+    return launch_k(kern, grid, dim3(256), 0, s, 1u, (const float *)A, a_rows, K, (const float *)B,
+                    (const float *)bias, N_out, row_gate, offsets, D.N, (float *)out);
+  }
   if (epi == 1)
-    return launch_k(ffn_simt_kernel<__nv_bfloat16, __nv_bfloat16, 1>, grid, dim3(256), 0, s, 1u,
-                    (const __nv_bfloat16 *)A, a_rows, K, (const __nv_bfloat16 *)B, (const __nv_bfloat16 *)bias, N_out,
-                    row_gate, offsets, D.N, (__nv_bfloat16 *)out);
-  return launch_k(ffn_simt_kernel<__nv_bfloat16, float, 2>, grid, dim3(256), 0, s, 1u, (const __nv_bfloat16 *)A, a_rows, K,
-                  (const __nv_bfloat16 *)B, (const __nv_bfloat16 *)bias, N_out, row_gate, offsets, D.N,
-                  (float *)out);
+    return launch_k(bound ? ffn_simt_kernel<__nv_bfloat16, __nv_bfloat16, 1, true>
+                          : ffn_simt_kernel<__nv_bfloat16, __nv_bfloat16, 1, false>,
+                    grid, dim3(256), 0, s, 1u, (const __nv_bfloat16 *)A, a_rows, K, (const __nv_bfloat16 *)B,
+                    (const __nv_bfloat16 *)bias, N_out, row_gate, offsets, D.N, (__nv_bfloat16 *)out);
+  return launch_k(bound ? ffn_simt_kernel<__nv_bfloat16, float, 2, true> : ffn_simt_kernel<__nv_bfloat16, float, 2, false>,
+                  grid, dim3(256), 0, s, 1u, (const __nv_bfloat16 *)A, a_rows, K, (const __nv_bfloat16 *)B,
+                  (const __nv_bfloat16 *)bias, N_out, row_gate, offsets, D.N, (float *)out);
 }
 
 }  // namespace moe

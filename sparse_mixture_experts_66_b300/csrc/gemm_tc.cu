@@ -77,6 +77,12 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+// 32-byte global store (one full sector per thread); p must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&v)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]), "r"(v[2]),
+               "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -456,32 +462,64 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();  // the TMEM load is warp-collective: reconverge after the row-masked stores
           tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BNP + col0), r);
           const int n = tl.ni * BNP + col0;
+          // h (bf16): one 32-byte store per 16 columns when its rows are
+          // 32-byte aligned (base aligned, d_ff a multiple of 16); y_perm
+          // (fp32): one 32-byte store per 8 columns when its base is (d is a
+          // multiple of 8); 16-byte stores otherwise
+          const bool wide_h = (d_ff & 15) == 0 && ((uintptr_t)h & 31) == 0;
+          const bool wide_y = ((uintptr_t)y_perm & 31) == 0;
 #pragma unroll
-          for (int g8 = 0; g8 < 4; ++g8) {
-            const bool store = valid && n + g8 * 8 < N_out;
-            const uint4 braw = sbias[cc * 4 + g8];
-            const uint32_t bw[4] = {braw.x, braw.y, braw.z, braw.w};
-            float2 v[4];  // accumulator + bias, column pairs
+          for (int g16 = 0; g16 < 2; ++g16) {
+            uint32_t pk[8];
+            float2 yv[2][4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              v[j] = __fadd2_rn(make_float2(__uint_as_float(r[g8 * 8 + 2 * j]), __uint_as_float(r[g8 * 8 + 2 * j + 1])),
-                                make_float2(__uint_as_float(bw[j] << 16), __uint_as_float(bw[j] & 0xffff0000u)));
-            if (tl.phase == 0) {
-              uint32_t pk[4];
+            for (int hh = 0; hh < 2; ++hh) {
+              const int g8 = g16 * 2 + hh;
+              const uint4 braw = sbias[cc * 4 + g8];
+              const uint32_t bw[4] = {braw.x, braw.y, braw.z, braw.w};
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
-                const float2 a = gelu_as2(v[j]);
-                __nv_bfloat162 h2 = __floats2bfloat162_rn(a.x, a.y);
-                pk[j] = *reinterpret_cast<uint32_t *>(&h2);
+                float2 v = __fadd2_rn(
+                    make_float2(__uint_as_float(r[g8 * 8 + 2 * j]), __uint_as_float(r[g8 * 8 + 2 * j + 1])),
+                    make_float2(__uint_as_float(bw[j] << 16), __uint_as_float(bw[j] & 0xffff0000u)));
+                if (tl.phase == 0) {
+                  const float2 a = gelu_as2(v);
+                  __nv_bfloat162 h2 = __floats2bfloat162_rn(a.x, a.y);
+                  pk[hh * 4 + j] = *reinterpret_cast<uint32_t *>(&h2);
+                } else {
+                  yv[hh][j] = __fmul2_rn(v, make_float2(g, g));
+                }
               }
-              if (store) *reinterpret_cast<uint4 *>(h + row * d_ff + n + g8 * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            } else if (store) {
-              const float2 g2 = make_float2(g, g);
+            }
+            const int nc = n + g16 * 16;  // first column of these 16
+            if (tl.phase == 0) {
+              if (!valid) continue;
+              __nv_bfloat16 *o = h + row * d_ff + nc;
+              if (wide_h && nc + 16 <= N_out) {
+                st_global_v8(o, pk);
+              } else {
+                if (nc < N_out) *reinterpret_cast<uint4 *>(o) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                if (nc + 8 < N_out) *reinterpret_cast<uint4 *>(o + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+              }
+            } else {
+              if (!valid) continue;
 #pragma unroll
-              for (int j = 0; j < 4; ++j) v[j] = __fmul2_rn(v[j], g2);
-              float *o = y_perm + row * d + n + g8 * 8;
-              *reinterpret_cast<float4 *>(o) = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
-              *reinterpret_cast<float4 *>(o + 4) = make_float4(v[2].x, v[2].y, v[3].x, v[3].y);
+              for (int hh = 0; hh < 2; ++hh) {
+                if (nc + hh * 8 >= N_out) continue;
+                float *o = y_perm + row * d + nc + hh * 8;
+                if (wide_y) {
+                  uint32_t w8[8];
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    w8[2 * j] = __float_as_uint(yv[hh][j].x);
+                    w8[2 * j + 1] = __float_as_uint(yv[hh][j].y);
+                  }
+                  st_global_v8(o, w8);
+                } else {
+                  *reinterpret_cast<float4 *>(o) = make_float4(yv[hh][0].x, yv[hh][0].y, yv[hh][1].x, yv[hh][1].y);
+                  *reinterpret_cast<float4 *>(o + 4) = make_float4(yv[hh][2].x, yv[hh][2].y, yv[hh][3].x, yv[hh][3].y);
+                }
+              }
             }
           }
         }

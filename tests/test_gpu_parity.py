@@ -174,6 +174,7 @@ E2E_CASES = [
     custom(48, 512, 2048, 8, 2, 1.0, router_bias="zipf", seed=14),  # drops
     custom(5, 768, 3072, 16, 4, math.inf, seed=15),  # fewer picks than experts
     custom(40, 520, 1000, 8, 2, 1.25, seed=16),  # ragged d and d_ff: partial k-blocks and weight tiles
+    custom(700, 136, 200, 4, 2, 1.25, seed=50),  # CTA-pair path, d_ff = 8 mod 16: 16-byte h stores
 ]
 
 
@@ -408,3 +409,25 @@ def test_expert_choice_against_oracle(w):
     scale = np.max(np.abs(y_ref[tok_ok]))
     err = np.max(np.abs(g["y"][tok_ok] - y_ref[tok_ok]))
     assert err <= parity.TOL[w.dtype] * scale, (err, scale)
+
+
+def test_expert_ffn_accepts_16_byte_aligned_outputs():
+    """h and y_perm only 16-byte aligned (the ABI's minimum): the same rows as
+    with the workspace's 256-byte aligned buffers, bit for bit."""
+    w = STAGE_CASES[0]
+    inp = draw(w)
+    g = parity.run_gpu(w, inp)
+    cfg, ws = g["_cfg"], g["_ws"]
+    v = ws.views()
+    R = ws.layout.rows
+    hb = torch.empty(R * w.d_ff * 2 + 32, dtype=torch.uint8, device="cuda")
+    yb = torch.empty(R * w.d * 4 + 32, dtype=torch.uint8, device="cuda")
+    h16 = hb[16:16 + R * w.d_ff * 2].view(torch.bfloat16).view(R, w.d_ff)
+    y16 = yb[16:16 + R * w.d * 4].view(torch.float32).view(R, w.d)
+    d = g["_dev"]
+    moe.moe_expert_ffn(cfg, v["x_perm"], v["offsets"], d["w1"], d["b1"], d["w2"], d["b2"], v["row_gate"], h16, y16,
+                       ws.buf)
+    ws.status()
+    rows = int(g["offsets"][-1])
+    assert torch.equal(h16[:rows], v["h"][:rows])
+    assert torch.equal(y16[:rows], v["y_perm"][:rows])
