@@ -83,6 +83,18 @@ __device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&v)[8]) {
                "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                : "memory");
 }
+// Bulk tensor store of a shared-memory box (issued by one thread), its group
+// commit, and the waits for the group's shared-memory reads / for completion.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
+               "r"(saddr(src)), "r"(c0), "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Ordinary shared-memory writes before a bulk copy reads them.
+__device__ __forceinline__ void fence_proxy_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -155,7 +167,10 @@ constexpr int kAP = BM * BK * 2;          // 16 KB: this CTA's 128 rows of A
 constexpr int kBP = 128 * BK * 2;         // 16 KB: this CTA's half of the B tile
 constexpr int kStageP = kAP + kBP;
 constexpr int BNP = 256;                  // pair tile width
-constexpr size_t kSmemP = 1024 + (size_t)kStagesP * kStageP + sizeof(Ctrl);
+// GEMM1 output staging: per epilogue warp one 32-row x 32-column bf16 box
+// (64 B rows, 64-byte swizzle) that a bulk tensor store writes to h
+constexpr int kStageOut = 32 * 32 * 2;
+constexpr size_t kSmemP = 1024 + (size_t)kStagesP * kStageP + (size_t)kEpiWarps * kStageOut + sizeof(Ctrl);
 
 struct PTile {
   int phase;  // 0: GEMM1, 1: GEMM2
@@ -190,6 +205,7 @@ __device__ __forceinline__ PTile decode_pair_tile(const Ctrl *c, int N_exp, int 
 __global__ void __launch_bounds__(kThreads, 1)
     ffn_pair_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w1,
                     const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w2,
+                    const __grid_constant__ CUtensorMap tm_hs,
                     const int32_t *__restrict__ offsets_g, int N_exp, int64_t R_max, int d, int d_ff,
                     const __nv_bfloat16 *__restrict__ b1, const __nv_bfloat16 *__restrict__ b2,
                     const float *__restrict__ row_gate, __nv_bfloat16 *__restrict__ h, float *__restrict__ y_perm,
@@ -198,7 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t *sA = base;
   uint8_t *sB = base + kStagesP * kAP;
-  Ctrl *c = (Ctrl *)(base + kStagesP * kStageP);
+  uint8_t *sOut = base + kStagesP * kStageP;  // 1024-byte aligned
+  Ctrl *c = (Ctrl *)(sOut + kEpiWarps * kStageOut);
   volatile int *abort = &c->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -455,22 +472,62 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
+        // GEMM1: this warp's 32 rows x 32 columns go through its staging box in
+        // shared memory to a bulk tensor store (full 64-byte row segments
+        // instead of 32 rows touched per store instruction)
+        uint8_t *box = sOut + (warp - 2) * kStageOut;
+        const int row0 = tl.m0 + (int)rank * BM + q * 32;
 #pragma unroll 1
         for (int cc = 0; cc < kCols / 32; ++cc) {
           const int col0 = part * kCols + cc * 32;
           uint32_t r[32];
           __syncwarp();  // the TMEM load is warp-collective: reconverge after the row-masked stores
           tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BNP + col0), r);
+          if (cc == kCols / 32 - 1) {  // the accumulator is read out: hand it back to the MMA issuer
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if (rank == 0) mbar_arrive(&c->tempty[acc]);
+              else mbar_arrive_cluster(acc == 0 ? tempty_leader0 : tempty_leader1);
+            }
+          }
           const int n = tl.ni * BNP + col0;
-          // h (bf16): one 32-byte store per 16 columns when its rows are
-          // 32-byte aligned (base aligned, d_ff a multiple of 16); y_perm
-          // (fp32): one 32-byte store per 8 columns when its base is (d is a
-          // multiple of 8); 16-byte stores otherwise
-          const bool wide_h = (d_ff & 15) == 0 && ((uintptr_t)h & 31) == 0;
+          if (tl.phase == 0) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int g8 = 0; g8 < 4; ++g8) {
+              const uint4 braw = sbias[cc * 4 + g8];
+              const uint32_t bw[4] = {braw.x, braw.y, braw.z, braw.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const float2 a = gelu_as2(__fadd2_rn(
+                    make_float2(__uint_as_float(r[g8 * 8 + 2 * j]), __uint_as_float(r[g8 * 8 + 2 * j + 1])),
+                    make_float2(__uint_as_float(bw[j] << 16), __uint_as_float(bw[j] & 0xffff0000u))));
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(a.x, a.y);
+                pk[g8 * 4 + j] = *reinterpret_cast<uint32_t *>(&h2);
+              }
+            }
+            if (lane == 0) bulk_wait_read0();  // the previous box has left the staging buffer
+            __syncwarp();
+            // row `lane`, 16-byte chunk j at chunk j ^ ((row >> 1) & 3): the
+            // 64-byte swizzle the store's tensor map names (and conflict-free)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              *reinterpret_cast<uint4 *>(box + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                  make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0 && n < N_out) {  // columns past d_ff are clipped by the store
+              tma_store_2d(&tm_hs, box, n, row0);
+              bulk_commit();
+            }
+            continue;
+          }
+          // y_perm (fp32): one 32-byte store per 8 columns when its base is
+          // 32-byte aligned (d is a multiple of 8); 16-byte stores otherwise
           const bool wide_y = ((uintptr_t)y_perm & 31) == 0;
 #pragma unroll
           for (int g16 = 0; g16 < 2; ++g16) {
-            uint32_t pk[8];
             float2 yv[2][4];
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
@@ -479,58 +536,52 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t bw[4] = {braw.x, braw.y, braw.z, braw.w};
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
-                float2 v = __fadd2_rn(
+                const float2 v = __fadd2_rn(
                     make_float2(__uint_as_float(r[g8 * 8 + 2 * j]), __uint_as_float(r[g8 * 8 + 2 * j + 1])),
                     make_float2(__uint_as_float(bw[j] << 16), __uint_as_float(bw[j] & 0xffff0000u)));
-                if (tl.phase == 0) {
-                  const float2 a = gelu_as2(v);
-                  __nv_bfloat162 h2 = __floats2bfloat162_rn(a.x, a.y);
-                  pk[hh * 4 + j] = *reinterpret_cast<uint32_t *>(&h2);
-                } else {
-                  yv[hh][j] = __fmul2_rn(v, make_float2(g, g));
-                }
+                yv[hh][j] = __fmul2_rn(v, make_float2(g, g));
               }
             }
             const int nc = n + g16 * 16;  // first column of these 16
-            if (tl.phase == 0) {
-              if (!valid) continue;
-              __nv_bfloat16 *o = h + row * d_ff + nc;
-              if (wide_h && nc + 16 <= N_out) {
-                st_global_v8(o, pk);
-              } else {
-                if (nc < N_out) *reinterpret_cast<uint4 *>(o) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                if (nc + 8 < N_out) *reinterpret_cast<uint4 *>(o + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-              }
-            } else {
-              if (!valid) continue;
+            if (!valid) continue;
 #pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                if (nc + hh * 8 >= N_out) continue;
-                float *o = y_perm + row * d + nc + hh * 8;
-                if (wide_y) {
-                  uint32_t w8[8];
+            for (int hh = 0; hh < 2; ++hh) {
+              if (nc + hh * 8 >= N_out) continue;
+              float *o = y_perm + row * d + nc + hh * 8;
+              if (wide_y) {
+                uint32_t w8[8];
 #pragma unroll
-                  for (int j = 0; j < 4; ++j) {
-                    w8[2 * j] = __float_as_uint(yv[hh][j].x);
-                    w8[2 * j + 1] = __float_as_uint(yv[hh][j].y);
-                  }
-                  st_global_v8(o, w8);
-                } else {
-                  *reinterpret_cast<float4 *>(o) = make_float4(yv[hh][0].x, yv[hh][0].y, yv[hh][1].x, yv[hh][1].y);
-                  *reinterpret_cast<float4 *>(o + 4) = make_float4(yv[hh][2].x, yv[hh][2].y, yv[hh][3].x, yv[hh][3].y);
+                for (int j = 0; j < 4; ++j) {
+                  w8[2 * j] = __float_as_uint(yv[hh][j].x);
+                  w8[2 * j + 1] = __float_as_uint(yv[hh][j].y);
                 }
+                st_global_v8(o, w8);
+              } else {
+                *reinterpret_cast<float4 *>(o) = make_float4(yv[hh][0].x, yv[hh][0].y, yv[hh][1].x, yv[hh][1].y);
+                *reinterpret_cast<float4 *>(o + 4) = make_float4(yv[hh][2].x, yv[hh][2].y, yv[hh][3].x, yv[hh][3].y);
               }
             }
           }
         }
       }
-      if (tl.phase == 0) fence_proxy_async_global();  // h stores before the GEMM2 tiles' TMA loads
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (rank == 0) mbar_arrive(&c->tempty[acc]);
-        else mbar_arrive_cluster(acc == 0 ? tempty_leader0 : tempty_leader1);
-        if (tl.phase == 0) red_release_add(blk_done + tl.blk, 1);
+      if (tl.swap) {  // (normal tiles handed the accumulator back after their last TMEM load)
+        if (tl.phase == 0) fence_proxy_async_global();  // h stores before the GEMM2 tiles' TMA loads
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (rank == 0) mbar_arrive(&c->tempty[acc]);
+          else mbar_arrive_cluster(acc == 0 ? tempty_leader0 : tempty_leader1);
+          if (tl.phase == 0) red_release_add(blk_done + tl.blk, 1);
+        }
+      } else if (tl.phase == 0) {
+        // the warp's bulk stores of h are complete before the block counter
+        // lets GEMM2 tiles load them
+        if (lane == 0) {
+          bulk_wait0();
+          fence_proxy_async_global();
+          red_release_add(blk_done + tl.blk, 1);
+        }
+        __syncwarp();
       }
       acc ^= 1;
       if (acc == 0) aph ^= 1u;
@@ -595,19 +646,19 @@ cudaError_t launch_ffn_tc(const Dims &D, const void *x_perm, int64_t a_rows, con
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  CUtensorMap tx, tw1, th, tw2;
+  CUtensorMap tx, tw1, th, tw2, ths;
   const uint64_t dx[2] = {(uint64_t)D.d, (uint64_t)a_rows};  // rows past a_rows read as zeros
   const uint64_t dw1[3] = {(uint64_t)D.d, (uint64_t)D.d_ff, (uint64_t)D.N};
   const uint64_t dh[2] = {(uint64_t)D.d_ff, (uint64_t)D.R_max};
   const uint64_t dw2[3] = {(uint64_t)D.d_ff, (uint64_t)D.d, (uint64_t)D.N};
   if (!make_map(&tx, x_perm, 2, dx, BM) || !make_map(&tw1, w1, 3, dw1, 128) || !make_map(&th, h, 2, dh, BM) ||
-      !make_map(&tw2, w2, 3, dw2, 128))
+      !make_map(&tw2, w2, 3, dw2, 128) || !make_map(&ths, h, 2, dh, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   const int64_t max_pairs = (int64_t)ffn_blocks_max(D) * (((D.d_ff + BNP - 1) / BNP) + ((D.d + BNP - 1) / BNP));
   int pairs = resident_pairs();
   if (max_pairs < pairs) pairs = (int)max_pairs;
   if (pairs < 1) pairs = 1;
-  return launch_k(ffn_pair_kernel, dim3(2 * pairs), dim3(kThreads), kSmemP, s, 2u, tx, tw1, th, tw2, offsets,
+  return launch_k(ffn_pair_kernel, dim3(2 * pairs), dim3(kThreads), kSmemP, s, 2u, tx, tw1, th, tw2, ths, offsets,
                   (int)D.N, (int64_t)D.R_max, (int)D.d, (int)D.d_ff, (const __nv_bfloat16 *)b1,
                   (const __nv_bfloat16 *)b2, row_gate, (__nv_bfloat16 *)h, y_perm, blk_done, (int)ffn_blocks_max(D),
                   status);

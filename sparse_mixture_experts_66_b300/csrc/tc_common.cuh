@@ -178,18 +178,20 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 tensor [outer..., inner] with a box of {64, box_rows(, 1)} and 128-byte
-// swizzle: the K-major operand tiles of the tensor-core kernels.
-inline bool make_map(CUtensorMap *m, const void *ptr, int rank, const uint64_t *dims, uint32_t box_rows) {
+// bf16 tensor [outer..., inner] with a box of {box_cols, box_rows(, 1)}; by
+// default {64, box_rows} with 128-byte swizzle, the K-major operand tiles of the
+// tensor-core kernels.
+inline bool make_map(CUtensorMap *m, const void *ptr, int rank, const uint64_t *dims, uint32_t box_rows,
+                     uint32_t box_cols = 64, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t gd[3], gs[2];
-  cuuint32_t box[3] = {64, box_rows, 1}, es[3] = {1, 1, 1};
+  cuuint32_t box[3] = {box_cols, box_rows, 1}, es[3] = {1, 1, 1};
   for (int i = 0; i < rank; ++i) gd[i] = dims[i];
   gs[0] = dims[0] * 2;
   if (rank == 3) gs[1] = dims[0] * dims[1] * 2;
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(ptr), gd, gs, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
