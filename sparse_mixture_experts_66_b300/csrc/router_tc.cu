@@ -8,12 +8,17 @@
 // rounded to bf16 ("Inside the Router", "Mixture of Experts: How Sparse
 // Routing Scales Transformers": router logits at higher precision).
 //
-// One CTA per 128 tokens: warp 0 streams the token tile [128 x 64] and the
-// W_g tile [NP x 64] per k-block with TMA (128-byte swizzle) through a small
-// ring; warp 1 issues tcgen05.mma (M=128, N=NP, K=16) into one TMEM
-// accumulator; warps 2-5 then own one token each (TMEM lane = token): they read
-// the token's logits 32 columns at a time and do the softmax and the top-k in
-// registers (the k best kept by an unrolled insertion, ties to the lower
+// S CTAs (a cluster of S) per 128 tokens, each over 1/S of d: warp 0 streams
+// the token tile [128 x 64] and the W_g tile [NP x 64] per k-block with TMA
+// (128-byte swizzle) through a small ring; warp 1 issues tcgen05.mma (M=128,
+// N=NP, K=16) into one TMEM accumulator. With S > 1 the epilogue warps of ranks
+// 1..S-1 copy their partial logits into rank 0's shared memory (distributed
+// shared memory), and after a cluster barrier rank 0 forms each logit as its
+// own partial plus ranks 1, 2, ... in that order: a fixed order, so the result
+// is deterministic. Splitting d lets a small batch stream x on S times as many
+// SMs. Rank 0's warps 2-5 then own one token each (TMEM lane = token): they
+// read the token's logits 32 columns at a time and do the softmax and the top-k
+// in registers (the k best kept by an unrolled insertion, ties to the lower
 // expert, picks in rank order). NP is N rounded up to 16..256; the W_g rows
 // past N are zero-filled by TMA and their columns are ignored.
 #include <math.h>
@@ -29,15 +34,27 @@ constexpr int kRM = 128;  // tokens per CTA (MMA M)
 constexpr int kRBK = 64;  // k-block: one 128-byte swizzle atom of bf16
 constexpr int kRThreads = 192;
 
-template <int NP> struct RCfg {
+template <int NP, int S> struct RCfg {
   static constexpr int kXBytes = kRM * kRBK * 2;
   static constexpr int kWBytes = NP * kRBK * 2;
   static constexpr int kStageBytes = kXBytes + kWBytes;
-  // as many stages as fit 192 KB (2..12): few CTAs stream all of x, so each
-  // needs many bytes in flight
-  static constexpr int kStages = (192 * 1024) / kStageBytes < 2 ? 2 : ((192 * 1024) / kStageBytes > 12 ? 12 : (192 * 1024) / kStageBytes);
+  // rank 0's buffer for the partial logits of ranks 1..S-1: [S-1][128][NP + 4]
+  // fp32 (rows 16-byte aligned; the +4 keeps a quarter-warp's 16-byte accesses
+  // on distinct banks)
+  static constexpr int kPartStride = NP + 4;
+  static constexpr int kPartBytes = S > 1 ? (S - 1) * kRM * kPartStride * 4 : 0;
+  // as many stages as fit 192 KB with the partials (2..12): few CTAs stream all
+  // of x, so each needs many bytes in flight
+  static constexpr int kFit = (192 * 1024 - kPartBytes) / kStageBytes;
+  static constexpr int kStages = kFit < 2 ? 2 : (kFit > 12 ? 12 : kFit);
   static constexpr int kTmemCols = NP < 32 ? 32 : NP;  // a power of two >= 32
 };
+
+// 16-byte store into another CTA's shared memory (a mapa'd address).
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
 
 struct RCtrl {
   unsigned long long full[12], empty[12], tfull, drain;
@@ -46,26 +63,32 @@ struct RCtrl {
   float bias[256];  // the logit bias (0 when none), for every padded expert column
 };
 
-template <int NP> constexpr size_t router_smem() {
-  return 1024 + (size_t)RCfg<NP>::kStages * RCfg<NP>::kStageBytes + sizeof(RCtrl);
+template <int NP, int S> constexpr size_t router_smem() {
+  using C = RCfg<NP, S>;
+  return 1024 + (size_t)C::kStages * C::kStageBytes + (size_t)C::kPartBytes + sizeof(RCtrl);
 }
 
-template <int NP>
+template <int NP, int S>
 __global__ void __launch_bounds__(kRThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                      const float *__restrict__ router_bias, int64_t T_, int d, int N, int k,
                      int32_t *__restrict__ topk_idx, float *__restrict__ gate, float *__restrict__ score,
                      float *__restrict__ probs, float *__restrict__ lse, int32_t *status) {
-  using C = RCfg<NP>;
+  using C = RCfg<NP, S>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t *sX = base;
   uint8_t *sW = base + C::kStages * C::kXBytes;
-  RCtrl *c = (RCtrl *)(base + C::kStages * C::kStageBytes);
+  float *part = (float *)(base + C::kStages * C::kStageBytes);
+  RCtrl *c = (RCtrl *)(base + C::kStages * C::kStageBytes + C::kPartBytes);
   volatile int *abort = &c->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t t0 = (int64_t)blockIdx.x * kRM;
-  const int kb_count = (d + kRBK - 1) / kRBK;
+  const uint32_t rank = S > 1 ? cluster_rank() : 0u;
+  const int64_t t0 = (int64_t)(blockIdx.x / S) * kRM;
+  // this rank's k-blocks: [r*kb/S, (r+1)*kb/S), at least two each (the host
+  // splits only when kb >= 2S)
+  const int kb_all = (d + kRBK - 1) / kRBK;
+  const int kb_lo = (int)rank * kb_all / S, kb_hi = ((int)rank + 1) * kb_all / S;
 
   if (warp == 1) {
     if (lane == 0) {
@@ -85,9 +108,11 @@ __global__ void __launch_bounds__(kRThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (S > 1) cluster_sync_all();  // rank 0 runs before its peers write into its shared memory
   tc_fence_after();
   const uint32_t tmem = c->tmem_base;
   pdl_wait();  // x and W_g may come from the previous kernel; the outputs may still be read by it
+  int epi_ok = 0;  // epilogue warps: this CTA's accumulator is complete
 
   if (warp == 0) {
     if (lane == 0) {
@@ -95,7 +120,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
       uint32_t ph = 0;
       uint32_t issued_mask = 0, parity_mask = 0;  // stages with a copy issued, and its phase parity
       bool ok = true;
-      for (int kb = 0; kb < kb_count; ++kb) {
+      for (int kb = kb_lo; kb < kb_hi; ++kb) {
         if (!mbar_wait_fast(&c->empty[s], ph ^ 1u, abort, status, kKRouter, 10 + s)) {
           ok = false;
           break;
@@ -126,7 +151,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
       bool ok = true, any = false;
       const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NP >> 3) << 17) |
                              ((uint32_t)(kRM >> 4) << 24);
-      for (int kb = 0; kb < kb_count; ++kb) {
+      for (int kb = kb_lo; kb < kb_hi; ++kb) {
         if (!mbar_wait_fast(&c->full[s], ph, abort, status, kKRouter, 20 + s)) {
           ok = false;
           break;
@@ -136,7 +161,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
         const uint64_t bd = smem_desc_sw128(saddr(sW + s * C::kWBytes));
 #pragma unroll
         for (int kk = 0; kk < kRBK / 16; ++kk)
-          umma_bf16_cta1(tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, (kb | kk) != 0 ? 1u : 0u);
+          umma_bf16_cta1(tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc,
+                         (kb != kb_lo || kk != 0) ? 1u : 0u);
         any = true;
         umma_commit_cta1(&c->empty[s]);
         if (++s == C::kStages) {
@@ -155,17 +181,80 @@ __global__ void __launch_bounds__(kRThreads, 1)
     }
   } else {
     const int q = warp & 3;
-    const int64_t t = t0 + q * 32 + lane;
+    const int row = q * 32 + lane;
     // the epilogue warps stage the logit bias (0 when none) while the MMAs run
     for (int i = threadIdx.x - 64; i < NP; i += kRThreads - 64)
       c->bias[i] = (router_bias && i < N) ? router_bias[i] : 0.f;
     asm volatile("bar.sync 1, %0;" ::"n"(kRThreads - 64) : "memory");  // the 4 epilogue warps only
-    int ok = 0;
-    if (lane == 0) ok = mbar_wait(&c->tfull, 0, abort, status, kKRouter, 30) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) {
+    if (lane == 0) epi_ok = mbar_wait(&c->tfull, 0, abort, status, kKRouter, 30) ? 1 : 0;
+    epi_ok = __shfl_sync(0xffffffffu, epi_ok, 0);
+    if (S > 1 && rank != 0 && epi_ok) {
+      // ranks 1..S-1: this warp's 32 rows of partial logits into rank 0's slot
       tc_fence_after();
       const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+      const uint32_t dst = map_to_rank(saddr(part + ((int)(rank - 1) * kRM + row) * C::kPartStride), 0);
+#pragma unroll 1
+      for (int c0 = 0; c0 < NP; c0 += 32) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(lane_base + (uint32_t)c0, r);
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          if (c0 + j < NP) st_cluster_v4(dst + (uint32_t)(c0 + j) * 4u, r[j], r[j + 1], r[j + 2], r[j + 3]);
+      }
+    }
+  }
+  if (S > 1) cluster_sync_all();  // the partials are in rank 0's shared memory
+
+  if (warp >= 2 && rank == 0 && epi_ok) {
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int64_t t = t0 + row;
+    {
+      tc_fence_after();
+      const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+      float *mine = part + row * C::kPartStride;  // rank 1's slot, reused for the summed logits
+      if (S > 1) {
+        // logit = own partial + rank 1 + rank 2 + ..., in that order
+#pragma unroll 1
+        for (int c0 = 0; c0 < NP; c0 += 32) {
+          uint32_t r[32];
+          __syncwarp();
+          tmem_ld32(lane_base + (uint32_t)c0, r);
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            if (c0 + j >= NP) break;
+            float4 a = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
+                                   __uint_as_float(r[j + 3]));
+#pragma unroll
+            for (int src = 0; src < S - 1; ++src) {
+              const float4 p = *reinterpret_cast<const float4 *>(part + (src * kRM + row) * C::kPartStride + c0 + j);
+              a.x += p.x;
+              a.y += p.y;
+              a.z += p.z;
+              a.w += p.w;
+            }
+            *reinterpret_cast<float4 *>(mine + c0 + j) = a;
+          }
+        }
+      }
+      // 32 logits of this token from column c0 (columns past NP read as 0)
+      auto load_chunk = [&](int c0, uint32_t(&r)[32]) {
+        if (S == 1) {
+          __syncwarp();  // the TMEM load is warp-collective
+          tmem_ld32(lane_base + (uint32_t)c0, r);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            const float4 v = c0 + j < NP ? *reinterpret_cast<const float4 *>(mine + c0 + j)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+            r[j] = __float_as_uint(v.x);
+            r[j + 1] = __float_as_uint(v.y);
+            r[j + 2] = __float_as_uint(v.z);
+            r[j + 3] = __float_as_uint(v.w);
+          }
+        }
+      };
       // pass 1: max and the k best (value desc, expert asc)
       float m = -INFINITY;
       float tv[8];
@@ -178,7 +267,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
 #pragma unroll 1
       for (int c0 = 0; c0 < NP; c0 += 32) {
         uint32_t r[32];
-        tmem_ld32(lane_base + (uint32_t)c0, r);
+        load_chunk(c0, r);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           int e = c0 + j;
@@ -203,7 +292,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
 #pragma unroll 1
       for (int c0 = 0; c0 < NP; c0 += 32) {
         uint32_t r[32];
-        tmem_ld32(lane_base + (uint32_t)c0, r);
+        load_chunk(c0, r);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int e = c0 + j;
@@ -217,8 +306,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
 #pragma unroll 1
         for (int c0 = 0; c0 < NP; c0 += 32) {
           uint32_t r[32];
-          __syncwarp();
-          tmem_ld32(lane_base + (uint32_t)c0, r);
+          load_chunk(c0, r);
           if (t < T_) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
@@ -258,13 +346,13 @@ __global__ void __launch_bounds__(kRThreads, 1)
   }
 }
 
-template <int NP>
+template <int NP, int S>
 cudaError_t launch_np(const Dims &D, const void *x, const void *w_g, const float *router_bias, int32_t *topk_idx,
                       float *gate, float *score, float *probs, float *lse, int32_t *status, cudaStream_t s) {
   static bool attr_set = false;
-  const size_t smem = router_smem<NP>();
+  const size_t smem = router_smem<NP, S>();
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(router_tc_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(router_tc_kernel<NP, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -273,9 +361,32 @@ cudaError_t launch_np(const Dims &D, const void *x, const void *w_g, const float
   const uint64_t dx[2] = {(uint64_t)D.d, (uint64_t)D.T};
   const uint64_t dw[2] = {(uint64_t)D.d, (uint64_t)D.N};
   if (!make_map(&tx, x, 2, dx, kRM) || !make_map(&tw, w_g, 2, dw, NP)) return cudaErrorInvalidValue;
-  const unsigned grid = (unsigned)((D.T + kRM - 1) / kRM);
-  return launch_k(router_tc_kernel<NP>, dim3(grid), dim3(kRThreads), smem, s, 1u, tx, tw, router_bias, D.T, (int)D.d,
-                  D.N, D.k, topk_idx, gate, score, probs, lse, status);
+  const unsigned grid = (unsigned)((D.T + kRM - 1) / kRM) * S;
+  return launch_k(router_tc_kernel<NP, S>, dim3(grid), dim3(kRThreads), smem, s, (unsigned)S, tx, tw, router_bias,
+                  D.T, (int)D.d, D.N, D.k, topk_idx, gate, score, probs, lse, status);
+}
+
+// CTAs per 128-token tile: split d over a cluster of 4 or 2 while the tiles
+// alone would leave most SMs idle and every rank keeps at least two k-blocks.
+// Only for NP <= 32: with more experts the per-token softmax and top-k, which
+// rank 0 alone runs, dominate the router and a split measured slower overall.
+int router_splits(const Dims &D, int NP) {
+  const int64_t tiles = (D.T + kRM - 1) / kRM;
+  const int kb = (int)((D.d + kRBK - 1) / kRBK);
+  if (NP > 32) return 1;
+  for (int S = 4; S >= 2; S >>= 1)
+    if (tiles * S <= num_sms() && kb >= 2 * S) return S;
+  return 1;
+}
+
+template <int NP>
+cudaError_t launch_split(const Dims &D, const void *x, const void *w_g, const float *router_bias, int32_t *topk_idx,
+                         float *gate, float *score, float *probs, float *lse, int32_t *status, cudaStream_t s) {
+  switch (router_splits(D, NP)) {
+    case 4: return launch_np<NP, 4>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
+    case 2: return launch_np<NP, 2>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
+    default: return launch_np<NP, 1>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
+  }
 }
 
 }  // namespace
@@ -284,11 +395,11 @@ cudaError_t launch_router_tc(const Dims &D, const void *x, const void *w_g, cons
                              int32_t *topk_idx, float *gate, float *score, float *probs, float *lse, int32_t *status,
                              cudaStream_t s) {
   if (D.dt != MOE_DT_BF16 || D.N > 256) return cudaErrorNotSupported;
-  if (D.N <= 16) return launch_np<16>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
-  if (D.N <= 32) return launch_np<32>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
-  if (D.N <= 64) return launch_np<64>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
-  if (D.N <= 128) return launch_np<128>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
-  return launch_np<256>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
+  if (D.N <= 16) return launch_split<16>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
+  if (D.N <= 32) return launch_split<32>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
+  if (D.N <= 64) return launch_np<64, 1>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
+  if (D.N <= 128) return launch_np<128, 1>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
+  return launch_np<256, 1>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
 }
 
 }  // namespace moe

@@ -139,8 +139,16 @@ def test_hidden_activations_within_bf16_rounding_of_exact_gelu(w):
     assert worst <= 0.0, worst
 
 
-def test_router_against_oracle():
-    w = custom(2048, 1024, 64, 8, 2, math.inf, seed=5)
+ROUTER_CASES = [
+    custom(2048, 1024, 64, 8, 2, math.inf, seed=5),  # d split over clusters of 4 CTAs
+    custom(1100, 512, 64, 32, 2, math.inf, seed=6),  # 32 experts, split of 4, ragged last tile
+    custom(1100, 512, 64, 64, 4, math.inf, router_bias="zipf", seed=7),  # 64 experts, k=4, no split
+    custom(2500, 384, 64, 16, 2, math.inf, seed=8),  # split of 2 (6 k-blocks)
+]
+
+
+@pytest.mark.parametrize("w", ROUTER_CASES, ids=lambda w: w.name)
+def test_router_against_oracle(w):
     inp = draw(w)
     g = parity.run_gpu(w, inp)
     ref = parity.oracle_ref(w, inp, sel=np.array([0]))
