@@ -71,40 +71,85 @@ template <> struct Store4<__nv_bfloat16> {
   }
 };
 
-// Combine, without K slices: a CTA owns U = 8 / KM tokens (KM >= k) and its
-// threads stride over their columns 4 at a time. A thread reads the U x KM
-// row indices once, then keeps U x KM 16-byte row loads in flight per column
-// group; the loads are unconditional (a dropped pick reads row 0 and is masked
-// out), so nothing serialises them, and no index division is needed. The
-// picks of a token are added in pick order.
-template <typename T, int KM>
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float *__restrict__ y_perm, int64_t d,
-                                                                  const int32_t *__restrict__ row_of,
-                                                                  const float *__restrict__ gate,
-                                                                  const T *__restrict__ x,
-                                                                  const float *__restrict__ y_shared, int64_t T_,
-                                                                  int k, int64_t R_max, uint32_t flags,
-                                                                  T *__restrict__ y, int32_t *status) {
+// W (4 or 8) consecutive values of a row as floats, loaded through the
+// read-only path, and stored back in the row's type.
+template <int W>
+__device__ __forceinline__ void ldv(const float *p, float (&v)[W]) {
+#pragma unroll
+  for (int i = 0; i < W; i += 4) {
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p + i));
+    v[i] = a.x; v[i + 1] = a.y; v[i + 2] = a.z; v[i + 3] = a.w;
+  }
+}
+template <int W>
+__device__ __forceinline__ void ldv(const __nv_bfloat16 *p, float (&v)[W]) {
+  uint32_t w[W / 2];
+  if (W == 8) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+    w[0] = u.x; w[1] = u.y; w[W / 2 - 2] = u.z; w[W / 2 - 1] = u.w;
+  } else {
+    const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p));
+    w[0] = u.x; w[W / 2 - 1] = u.y;
+  }
+#pragma unroll
+  for (int i = 0; i < W / 2; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+template <int W>
+__device__ __forceinline__ void stv(float *p, const float (&v)[W]) {
+#pragma unroll
+  for (int i = 0; i < W; i += 4) *reinterpret_cast<float4 *>(p + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+}
+template <int W>
+__device__ __forceinline__ void stv(__nv_bfloat16 *p, const float (&v)[W]) {
+  uint32_t w[W / 2];
+#pragma unroll
+  for (int i = 0; i < W / 2; ++i) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t *>(&h);
+  }
+  if (W == 8) *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[W / 2 - 2], w[W / 2 - 1]);
+  else *reinterpret_cast<uint2 *>(p) = make_uint2(w[0], w[W / 2 - 1]);
+}
+
+// Combine, without K slices: a CTA owns U = 8 / KM tokens (KM >= k); its
+// threads take W columns at a time (8 for bf16, 4 for fp32). The
+// CTA reads the U x KM row indices once and turns them into source-row
+// pointers (null for a dropped pick), so the column loop holds no index
+// arithmetic, and every condition in it is uniform across the CTA. A thread
+// keeps up to U x KM x W / 4 16-byte loads in flight. The picks of a token are
+// added in pick order.
+constexpr int kC8Threads = 128;
+template <typename T, int KM, int W>
+__global__ void __launch_bounds__(kC8Threads) combine_kernel(const float *__restrict__ y_perm, int64_t d,
+                                                             const int32_t *__restrict__ row_of,
+                                                             const float *__restrict__ gate,
+                                                             const T *__restrict__ x,
+                                                             const float *__restrict__ y_shared, int64_t T_, int k,
+                                                             int64_t R_max, uint32_t flags, T *__restrict__ y,
+                                                             int32_t *status) {
   pdl_wait();
   constexpr int U = 8 / KM;
   const int64_t t0 = (int64_t)blockIdx.x * U;
-  int64_t rows[U][KM];  // row of each pick, or -1 (dropped / out of range)
-  float ksum[U];        // kept-gate sum (for MOE_FLAG_RENORM_SURVIVORS)
-  bool renorm[U];       // divide by ksum
-  bool ident[U];        // identity fallback: every pick dropped
+  const float *src[U][KM];  // source row of each kept pick, or null
+  float ksum[U];            // kept-gate sum (for MOE_FLAG_RENORM_SURVIVORS)
+  bool live[U], renorm[U], ident[U];
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     const int64_t t = t0 + u;
+    live[u] = t < T_;
     int nkept = 0;
     float kept_gate = 0.f;
 #pragma unroll
     for (int j = 0; j < KM; ++j) {
-      int32_t r = (t < T_ && j < k) ? __ldg(row_of + t * k + j) : -1;
+      int32_t r = (live[u] && j < k) ? __ldg(row_of + t * k + j) : -1;
       if (r >= R_max) {
         if (threadIdx.x == 0) report_error(status, MOE_ERR_BOUNDS, kKCombine, (int32_t)t);
         r = -1;
       }
-      rows[u][j] = r;
+      src[u][j] = r >= 0 ? y_perm + (int64_t)r * d : nullptr;
       if (r >= 0) {
         ++nkept;
         if (flags & MOE_FLAG_RENORM_SURVIVORS) kept_gate += __ldg(gate + t * k + j);
@@ -114,41 +159,41 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float *_
     renorm[u] = (flags & MOE_FLAG_RENORM_SURVIVORS) && nkept > 0;
     ident[u] = (flags & MOE_FLAG_IDENTITY_FALLBACK) && nkept == 0;
   }
-  for (int64_t c = (int64_t)threadIdx.x * 4; c < d; c += kCombineThreads * 4) {
-    float4 v[U][KM];
+  for (int64_t c = (int64_t)threadIdx.x * W; c < d; c += kC8Threads * W) {
+    float v[U][KM][W];
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
-      for (int j = 0; j < KM; ++j)
-        v[u][j] = __ldg(reinterpret_cast<const float4 *>(y_perm + (rows[u][j] >= 0 ? rows[u][j] : 0) * d + c));
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if (t0 + u >= T_) continue;
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
       for (int j = 0; j < KM; ++j) {
-        if (rows[u][j] >= 0) {
-          a.x += v[u][j].x;
-          a.y += v[u][j].y;
-          a.z += v[u][j].z;
-          a.w += v[u][j].w;
+        if (src[u][j]) {
+          ldv<W>(src[u][j] + c, v[u][j]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < W; ++i) v[u][j][i] = 0.f;
         }
       }
-      if (renorm[u]) {
-        a.x /= ksum[u];
-        a.y /= ksum[u];
-        a.z /= ksum[u];
-        a.w /= ksum[u];
-      }
-      if (ident[u]) a = Store4<T>::ld(x + (t0 + u) * d + c);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (!live[u]) continue;
+      float a[W];
+#pragma unroll
+      for (int i = 0; i < W; ++i) a[i] = 0.f;
+#pragma unroll
+      for (int j = 0; j < KM; ++j)
+        if (src[u][j])
+#pragma unroll
+          for (int i = 0; i < W; ++i) a[i] += v[u][j][i];
+      if (renorm[u])
+#pragma unroll
+        for (int i = 0; i < W; ++i) a[i] /= ksum[u];
+      if (ident[u]) ldv<W>(x + (t0 + u) * d + c, a);
       if (y_shared) {  // the shared expert, added last
-        const float4 sh = __ldg(reinterpret_cast<const float4 *>(y_shared + (t0 + u) * d + c));
-        a.x += sh.x;
-        a.y += sh.y;
-        a.z += sh.z;
-        a.w += sh.w;
+        float sh[W];
+        ldv<W>(y_shared + (t0 + u) * d + c, sh);
+#pragma unroll
+        for (int i = 0; i < W; ++i) a[i] += sh[i];
       }
-      Store4<T>::st(y + (t0 + u) * d + c, a);
+      stv<W>(y + (t0 + u) * d + c, a);
     }
   }
 }
@@ -306,9 +351,14 @@ cudaError_t launch_combine_t(const Dims &D, const float *y_perm, const float *y_
   const int km = D.k <= 1 ? 1 : D.k <= 2 ? 2 : D.k <= 4 ? 4 : 8;
   const int64_t tok_per_block = 8 / km;
   const unsigned g = (unsigned)((D.T + tok_per_block - 1) / tok_per_block);
-  auto kern = km == 1 ? combine_kernel<T, 1> : km == 2 ? combine_kernel<T, 2> : km == 4 ? combine_kernel<T, 4>
-                                                                                    : combine_kernel<T, 8>;
-  return launch_k(kern, dim3(g), dim3(kCombineThreads), 0, s, 1u, y_perm, D.d, row_of, gate, x, y_shared, D.T, D.k,
+  // bf16: 8 columns (16-byte loads and stores); fp32: 4 (16-byte loads, and
+  // twice the active threads on narrow rows)
+  const bool w8 = sizeof(T) == 2;
+  auto kern = km == 1   ? (w8 ? combine_kernel<T, 1, 8> : combine_kernel<T, 1, 4>)
+              : km == 2 ? (w8 ? combine_kernel<T, 2, 8> : combine_kernel<T, 2, 4>)
+              : km == 4 ? (w8 ? combine_kernel<T, 4, 8> : combine_kernel<T, 4, 4>)
+                        : (w8 ? combine_kernel<T, 8, 8> : combine_kernel<T, 8, 4>);
+  return launch_k(kern, dim3(g), dim3(kC8Threads), 0, s, 1u, y_perm, D.d, row_of, gate, x, y_shared, D.T, D.k,
                   D.R_max, D.flags, y, status);
 }
 }  // namespace
