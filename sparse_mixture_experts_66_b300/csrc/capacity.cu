@@ -243,6 +243,19 @@ __global__ void __launch_bounds__(kThreads) capacity_kernel(
     }
     int tot_kept;
     int slot = block_exclusive_scan(my_kept, s_warp, &tot_kept) + run_kept;
+    // token of each request: one division per thread, then steps (a division
+    // per matching request would run once per item slot in a divergent warp)
+    int64_t tq = i0 / k;
+    int rq = (int)(i0 - tq * k);
+    int32_t tok[kItems];
+#pragma unroll
+    for (int q = 0; q < kItems; ++q) {
+      tok[q] = (int32_t)tq;
+      if (++rq == k) {
+        rq = 0;
+        ++tq;
+      }
+    }
 #pragma unroll
     for (int q = 0; q < kItems; ++q) {
       if (it.ie[q] != e) continue;
@@ -253,7 +266,7 @@ __global__ void __launch_bounds__(kThreads) capacity_kernel(
       } else if (kept[q]) {
         const int64_t r = off + slot;
         row_of[i] = (int32_t)r;
-        row_token[r] = (int32_t)(i / k);
+        row_token[r] = tok[q];
         row_gate[r] = it.g[q];
         ++slot;
       } else {
