@@ -22,9 +22,9 @@
  *     16-byte aligned. The library never allocates or frees device memory.
  *   - Weights use the [out, in] layout of a linear layer: W_g [N, d],
  *     W1 [N, d_ff, d], b1 [N, d_ff], W2 [N, d, d_ff], b2 [N, d].
- *   - x, W_g, W1, b1, W2, b2, x_perm, h and y are in the configured dtype
- *     (fp32 or bf16); router outputs, gates, y_perm and the logit bias are
- *     fp32; indices are int32.
+ *   - x, W_g, W1, b1, W2, b2, x_perm, h, y_perm and y are in the configured
+ *     dtype (fp32 or bf16); router outputs, gates and the logit bias are fp32;
+ *     indices are int32.
  *   - Calls enqueue work on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and return without synchronising. Argument errors are detected
  *     on the host and returned before anything is enqueued. Errors found by
@@ -131,7 +131,7 @@ typedef struct {
   size_t row_gate;    /* fp32  [rows]  combine weight of each permuted row, 0 for padding */
   size_t x_perm;      /* dtype [rows, d]    tokens gathered per expert */
   size_t h;           /* dtype [rows, d_ff] expert hidden activations */
-  size_t y_perm;      /* fp32  [rows, d]    gate-scaled expert outputs */
+  size_t y_perm;      /* dtype [rows, d]    gate-scaled expert outputs */
   size_t y_split;     /* fp32  [S-1, rows, d] decode-shaped configs only: the second GEMM's extra K slices */
   size_t ffn_sync;    /* int32 bf16 configs: completion counters of h tiles (per expert in decode-shaped
                        * configs, else per 256-row block) and an exit count, read by the fused expert
@@ -142,7 +142,7 @@ typedef struct {
   size_t shared_offsets; /* int32 [2]  MOE_FLAG_SHARED_EXPERT only: the shared expert's one segment */
   size_t h_shared;    /* dtype [Tp, d_ff] MOE_FLAG_SHARED_EXPERT only: its hidden activations, Tp = T
                        * rounded up to 128 */
-  size_t y_shared;    /* fp32  [Tp, d]    MOE_FLAG_SHARED_EXPERT only: its output */
+  size_t y_shared;    /* dtype [Tp, d]    MOE_FLAG_SHARED_EXPERT only: its output */
   size_t shared_sync; /* int32        MOE_FLAG_SHARED_EXPERT only: completion counters of its FFN */
   size_t total;       /* bytes of the whole workspace */
   int64_t rows;       /* R_max */
@@ -216,20 +216,20 @@ moe_status moe_dispatch(const moe_config *cfg, const void *x, const int32_t *top
 
 /* Step 6: the expert FFNs over the permuted rows, two grouped GEMMs.
  *   h[r]      = GELU(x_perm[r] W1[e]^T + b1[e])                (dtype)
- *   y_perm[r] = row_gate[r] * (h[r] W2[e]^T + b2[e])           (fp32)
+ *   y_perm[r] = row_gate[r] * (h[r] W2[e]^T + b2[e])           (dtype)
  * for every row r of expert e's segment [offsets[e], offsets[e+1]).
  *   row_gate may be NULL (no scaling). h [rows, d_ff] may be NULL to use the
  *   workspace's h buffer. Accumulation is fp32 (bf16 inputs: tensor cores,
  *   tcgen05, accumulating in tensor memory). For decode-shaped configs (bf16,
  *   T*k <= 64*N) the second GEMM is split along d_ff: y_perm receives the
- *   first slice and the workspace's y_split the others, which moe_combine
+ *   first slice and the workspace's y_split (fp32) the others, which moe_combine
  *   (given the same workspace) adds in slice order. For bf16 configs both
  *   GEMMs run in one launch, whose second-GEMM tiles wait (bounded,
  *   MOE_ERR_TIMEOUT) on completion counters in the workspace's ffn_sync
  *   (zero on entry; the launch's last CTA leaves them zero). */
 moe_status moe_expert_ffn(const moe_config *cfg, const void *x_perm, const int32_t *offsets, const void *w1,
                           const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
-                          float *y_perm, void *ws, moe_stream_t stream);
+                          void *y_perm, void *ws, moe_stream_t stream);
 
 /* The shared expert over every token: y_shared[t] = W2s GELU(W1s x_t + b1s)
  * + b2s into the workspace of a cfg with MOE_FLAG_SHARED_EXPERT (x [T, d],
@@ -240,7 +240,7 @@ moe_status moe_shared_expert(const moe_config *cfg, const void *x, const void *s
                              const void *sw2, const void *sb2, void *ws, moe_stream_t stream);
 
 /* Step 7: y[t] = sum over j < k with row_of[t,j] >= 0, in j order, of
- * y_perm[row_of[t,j]], in fp32, stored in dtype. No atomics. For
+ * y_perm[row_of[t,j]], added in fp32 and rounded once to dtype. No atomics. For
  * decode-shaped configs each pick's term is first completed with the same row
  * of the workspace's y_split slices, added in slice order.
  *   gate [T, k] is read only under MOE_FLAG_RENORM_SURVIVORS (the sum is then
@@ -248,7 +248,7 @@ moe_status moe_shared_expert(const moe_config *cfg, const void *x, const void *s
  *   MOE_FLAG_IDENTITY_FALLBACK (a token with no kept pick outputs x_t). Either
  *   may be NULL otherwise. Under MOE_FLAG_SHARED_EXPERT the workspace's
  *   y_shared row is added last. ws: a workspace of cfg (status word). */
-moe_status moe_combine(const moe_config *cfg, const float *y_perm, const int32_t *row_of, const float *gate,
+moe_status moe_combine(const moe_config *cfg, const void *y_perm, const int32_t *row_of, const float *gate,
                        const void *x, void *y, void *ws, moe_stream_t stream);
 
 /* moe_forward plus the shared expert (cfg must carry MOE_FLAG_SHARED_EXPERT):

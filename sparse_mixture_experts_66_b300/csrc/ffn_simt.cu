@@ -5,7 +5,7 @@
 // Rows of the permuted buffer are grouped by expert in segments that start on
 // multiples of 128 rows, so a 64-row tile belongs to exactly one expert.
 //   epilogue 1: out = GELU(acc + b1[e])                   (first GEMM)
-//   epilogue 2: out = row_gate[r] * (acc + b2[e])         (second GEMM, fp32)
+//   epilogue 2: out = row_gate[r] * (acc + b2[e])         (second GEMM, in x's dtype)
 // fp32 is kept on CUDA cores on purpose: tf32 tensor cores round the inputs
 // to a 10-bit mantissa, which cannot meet a 1e-4 relative bound.
 #include "moe_internal.cuh"
@@ -99,9 +99,10 @@ cudaError_t launch_ffn_simt(const Dims &D, int epi, const void *A, int64_t a_row
                           : ffn_simt_kernel<__nv_bfloat16, __nv_bfloat16, 1, false>,
                     grid, dim3(256), 0, s, 1u, (const __nv_bfloat16 *)A, a_rows, K, (const __nv_bfloat16 *)B,
                     (const __nv_bfloat16 *)bias, N_out, row_gate, offsets, D.N, (__nv_bfloat16 *)out);
-  return launch_k(bound ? ffn_simt_kernel<__nv_bfloat16, float, 2, true> : ffn_simt_kernel<__nv_bfloat16, float, 2, false>,
+  return launch_k(bound ? ffn_simt_kernel<__nv_bfloat16, __nv_bfloat16, 2, true>
+                        : ffn_simt_kernel<__nv_bfloat16, __nv_bfloat16, 2, false>,
                   grid, dim3(256), 0, s, 1u, (const __nv_bfloat16 *)A, a_rows, K, (const __nv_bfloat16 *)B,
-                  (const __nv_bfloat16 *)bias, N_out, row_gate, offsets, D.N, (float *)out);
+                  (const __nv_bfloat16 *)bias, N_out, row_gate, offsets, D.N, (__nv_bfloat16 *)out);
 }
 
 }  // namespace moe

@@ -20,7 +20,8 @@
 // one of two TMEM accumulators; warps 2-5 read one accumulator lane each
 // (TMEM lane = weight row f) and store the 64 token values of that row:
 //   GEMM1: h[off_e + j, f]      = GELU(D^T[f, j] + b1[e][f])          (bf16)
-//   GEMM2: y_s[off_e + j, o]    = g_j * (D^T[o, j] + [s == 0] b2[e][o]) (fp32)
+//   GEMM2: y_s[off_e + j, o]    = g_j * (D^T[o, j] + [s == 0] b2[e][o])
+//          (slice 0 into y_perm as bf16, slices 1..S-1 into y_split as fp32)
 // GEMM2 splits K into S slices (s = 0..S-1) to give every SM work; slice s
 // writes its own partial buffer and the combine adds the S partials in a
 // fixed order, so the result stays deterministic. A GEMM2 tile of expert e
@@ -94,7 +95,8 @@ __global__ void __launch_bounds__(kDThreads, 1)
                       const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_h,
                       const int32_t *__restrict__ offsets_g, int N_exp, int64_t R_max, int d, int d_ff, int S,
                       const __nv_bfloat16 *__restrict__ b1, const __nv_bfloat16 *__restrict__ b2,
-                      const float *__restrict__ row_gate, __nv_bfloat16 *__restrict__ h, float *__restrict__ y_perm,
+                      const float *__restrict__ row_gate, __nv_bfloat16 *__restrict__ h,
+                      __nv_bfloat16 *__restrict__ y_perm,
                       float *__restrict__ y_split, int32_t *__restrict__ h_done, int32_t *status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -306,7 +308,8 @@ __global__ void __launch_bounds__(kDThreads, 1)
         gate_lo = row_gate[tl.row0 + lane];
         gate_hi = row_gate[tl.row0 + 32 + lane];
       }
-      float *dst = tl.phase ? (tl.sp == 0 ? y_perm : y_split + (int64_t)(tl.sp - 1) * R_max * d) : nullptr;
+      // K slice 0 goes to y_perm (bf16), slices 1..S-1 to y_split (fp32)
+      float *dst = tl.phase && tl.sp > 0 ? y_split + (int64_t)(tl.sp - 1) * R_max * d : nullptr;
       int ok = 0;
       if (lane == 0) ok = mbar_wait(&c->tfull[acc], aph, abort, status, kKGemmTcDecode, 40 + acc) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -334,7 +337,11 @@ __global__ void __launch_bounds__(kDThreads, 1)
           for (int j = 0; j < 32; ++j) {
             const int64_t row = (int64_t)tl.row0 + c0 + j;
             const float g = __shfl_sync(0xffffffffu, gsrc, j);
-            if (fvalid) dst[row * d + f] = g * (__uint_as_float(r[j]) + b);
+            if (fvalid) {
+              const float v = g * (__uint_as_float(r[j]) + b);
+              if (tl.sp == 0) y_perm[row * d + f] = __float2bfloat16_rn(v);
+              else dst[row * d + f] = v;
+            }
           }
         }
       }
@@ -432,7 +439,7 @@ int decode_splits(const Dims &D) {
 
 cudaError_t launch_ffn_decode(const Dims &D, const void *x_perm, const int32_t *offsets, const void *w1,
                               const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
-                              float *y_perm, float *y_split, int32_t *h_done, int32_t *status, cudaStream_t s) {
+                              void *y_perm, float *y_split, int32_t *h_done, int32_t *status, cudaStream_t s) {
   const int S = decode_splits(D);
   if (S < 1 || (S > 1 && !y_split) || !h_done || D.N > kDMaxExperts) return cudaErrorNotSupported;
   static bool attr_set = false;
@@ -458,7 +465,8 @@ cudaError_t launch_ffn_decode(const Dims &D, const void *x_perm, const int32_t *
   // are resident together: a GEMM2 tile never waits on a CTA that cannot run.
   return launch_k(ffn_decode_kernel, dim3((unsigned)grid), dim3(kDThreads), kDSmem, s, 1u, tw1, tx, tw2, th, offsets,
                   (int)D.N, (int64_t)D.R_max, (int)D.d, (int)D.d_ff, S, (const __nv_bfloat16 *)b1,
-                  (const __nv_bfloat16 *)b2, row_gate, (__nv_bfloat16 *)h, y_perm, y_split, h_done, status);
+                  (const __nv_bfloat16 *)b2, row_gate, (__nv_bfloat16 *)h, (__nv_bfloat16 *)y_perm, y_split, h_done,
+                  status);
 }
 
 }  // namespace moe

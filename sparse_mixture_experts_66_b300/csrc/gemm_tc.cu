@@ -8,7 +8,7 @@
 // second GEMM's epilogue.
 //   GEMM1: h[r, :]      = GELU(x_perm[r] . W1[e]^T + b1[e])         -> bf16
 //          (GELU via the Abramowitz & Stegun 7.1.26 erf, |error| <= 1.5e-7)
-//   GEMM2: y_perm[r, :] = row_gate[r] * (h[r] . W2[e]^T + b2[e])    -> fp32
+//   GEMM2: y_perm[r, :] = row_gate[r] * (h[r] . W2[e]^T + b2[e])    -> bf16
 // for the rows r of expert e's segment. Segments start on multiples of 128
 // rows, so each 128-row half tile belongs to one expert and uses one weight
 // matrix.
@@ -28,7 +28,9 @@
 //             accumulators and multicasts the commits to both CTAs;
 //   warps 2-9 epilogue: tcgen05.ld of the CTA's 128 finished rows (warp w
 //             reads TMEM lanes 32*(w%4)...; two warps per lane quarter split
-//             the columns), bias + GELU or bias + gate scale, global stores;
+//             the columns), bias + GELU -> h (bf16 boxes staged in shared
+//             memory, written by bulk tensor stores) or bias x gate -> y_perm
+//             (bf16, 32-byte stores from registers);
 //             then the accumulator is handed back to the leader, so the
 //             epilogue of tile i overlaps the MMAs of tile i+1.
 // Every wait is bounded: after kTimeoutNs the kernel records MOE_ERR_TIMEOUT,
@@ -67,7 +69,7 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 // 32-byte global store (one full sector per thread); p must be 32-byte aligned.
-__device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&v)[8]) {
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t *v) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]), "r"(v[2]),
                "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                : "memory");
@@ -194,7 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tm_hs,
                     const int32_t *__restrict__ offsets_g, int N_exp, int64_t R_max, int d, int d_ff,
                     const __nv_bfloat16 *__restrict__ b1, const __nv_bfloat16 *__restrict__ b2,
-                    const float *__restrict__ row_gate, __nv_bfloat16 *__restrict__ h, float *__restrict__ y_perm,
+                    const float *__restrict__ row_gate, __nv_bfloat16 *__restrict__ h,
+                    __nv_bfloat16 *__restrict__ y_perm,
                     int32_t *__restrict__ blk_done, int nblk_max, int32_t *status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -453,14 +456,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const float gj = __shfl_sync(0xffffffffu, gsrc, j);
-              if (fvalid) y_perm[((int64_t)tl.m0 + c0 + j) * d + f] = gj * (__uint_as_float(r[j]) + bsw);
+              if (fvalid)
+                y_perm[((int64_t)tl.m0 + c0 + j) * d + f] = __float2bfloat16_rn(gj * (__uint_as_float(r[j]) + bsw));
             }
           }
         }
       } else {
-        // GEMM1: this warp's 32 rows x 32 columns go through its staging box in
-        // shared memory to a bulk tensor store (full 64-byte row segments
-        // instead of 32 rows touched per store instruction)
+        // GEMM1: this warp's 32 rows x 32 columns (bf16) go through its staging
+        // box in shared memory to a bulk tensor store into h: full 64-byte row
+        // segments instead of 32 rows touched per store instruction (the h
+        // epilogue paces GEMM1 otherwise)
         uint8_t *box = sOut + (warp - 2) * kStageOut;
         const int row0 = tl.m0 + (int)rank * BM + q * 32;
 #pragma unroll 1
@@ -478,8 +483,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           const int n = tl.ni * BNP + col0;
+          // GEMM1: GELU(acc + b1); GEMM2: gate * (acc + b2); both to bf16 (two
+          // loops, so GEMM2 tiles never evaluate the GELU)
+          uint32_t pk[16];
           if (tl.phase == 0) {
-            uint32_t pk[16];
 #pragma unroll
             for (int g8 = 0; g8 < 4; ++g8) {
               const uint4 braw = sbias[cc * 4 + g8];
@@ -493,60 +500,58 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pk[g8 * 4 + j] = *reinterpret_cast<uint32_t *>(&h2);
               }
             }
-            if (lane == 0) bulk_wait_read0();  // the previous box has left the staging buffer
-            __syncwarp();
-            // row `lane`, 16-byte chunk j at chunk j ^ ((row >> 1) & 3): the
-            // 64-byte swizzle the store's tensor map names (and conflict-free)
+          } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              *reinterpret_cast<uint4 *>(box + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
-                  make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-            fence_proxy_async_shared();
-            __syncwarp();
-            if (lane == 0 && n < N_out) {  // columns past d_ff are clipped by the store
-              tma_store_2d(&tm_hs, box, n, row0);
-              bulk_commit();
-            }
-            continue;
-          }
-          // y_perm (fp32): one 32-byte store per 8 columns when its base is
-          // 32-byte aligned (d is a multiple of 8); 16-byte stores otherwise
-          const bool wide_y = ((uintptr_t)y_perm & 31) == 0;
-#pragma unroll
-          for (int g16 = 0; g16 < 2; ++g16) {
-            float2 yv[2][4];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              const int g8 = g16 * 2 + hh;
+            for (int g8 = 0; g8 < 4; ++g8) {
               const uint4 braw = sbias[cc * 4 + g8];
               const uint32_t bw[4] = {braw.x, braw.y, braw.z, braw.w};
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
-                const float2 v = __fadd2_rn(
-                    make_float2(__uint_as_float(r[g8 * 8 + 2 * j]), __uint_as_float(r[g8 * 8 + 2 * j + 1])),
-                    make_float2(__uint_as_float(bw[j] << 16), __uint_as_float(bw[j] & 0xffff0000u)));
-                yv[hh][j] = __fmul2_rn(v, make_float2(g, g));
+                const float2 a = __fmul2_rn(
+                    __fadd2_rn(make_float2(__uint_as_float(r[g8 * 8 + 2 * j]), __uint_as_float(r[g8 * 8 + 2 * j + 1])),
+                               make_float2(__uint_as_float(bw[j] << 16), __uint_as_float(bw[j] & 0xffff0000u))),
+                    make_float2(g, g));
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(a.x, a.y);
+                pk[g8 * 4 + j] = *reinterpret_cast<uint32_t *>(&h2);
               }
             }
-            const int nc = n + g16 * 16;  // first column of these 16
-            if (!valid) continue;
+          }
+          if (tl.phase == 1) {
+            // y_perm straight from registers: GEMM2 tiles wait on operand
+            // delivery, and bulk stores would share the TMA unit with their
+            // loads. One 32-byte store per 16 columns when the rows are 32-byte
+            // aligned (base aligned, d a multiple of 16), else 16-byte stores.
+            const bool wide_y = (d & 15) == 0 && ((uintptr_t)y_perm & 31) == 0;
+            if (valid) {
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              if (nc + hh * 8 >= N_out) continue;
-              float *o = y_perm + row * d + nc + hh * 8;
-              if (wide_y) {
-                uint32_t w8[8];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  w8[2 * j] = __float_as_uint(yv[hh][j].x);
-                  w8[2 * j + 1] = __float_as_uint(yv[hh][j].y);
+              for (int hf = 0; hf < 2; ++hf) {
+                const int nc = n + 16 * hf;
+                __nv_bfloat16 *o = y_perm + row * d + nc;
+                if (wide_y && nc + 16 <= N_out) {
+                  st_global_v8(o, pk + 8 * hf);
+                } else {
+                  if (nc < N_out)
+                    *reinterpret_cast<uint4 *>(o) = make_uint4(pk[8 * hf], pk[8 * hf + 1], pk[8 * hf + 2], pk[8 * hf + 3]);
+                  if (nc + 8 < N_out)
+                    *reinterpret_cast<uint4 *>(o + 8) = make_uint4(pk[8 * hf + 4], pk[8 * hf + 5], pk[8 * hf + 6], pk[8 * hf + 7]);
                 }
-                st_global_v8(o, w8);
-              } else {
-                *reinterpret_cast<float4 *>(o) = make_float4(yv[hh][0].x, yv[hh][0].y, yv[hh][1].x, yv[hh][1].y);
-                *reinterpret_cast<float4 *>(o + 4) = make_float4(yv[hh][2].x, yv[hh][2].y, yv[hh][3].x, yv[hh][3].y);
               }
             }
+            continue;
+          }
+          if (lane == 0) bulk_wait_read0();  // the previous box has left the staging buffer
+          __syncwarp();
+          // row `lane`, 16-byte chunk j at chunk j ^ ((row >> 1) & 3): the
+          // 64-byte swizzle the store's tensor map names (and conflict-free)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4 *>(box + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0 && n < N_out) {  // columns past d_ff are clipped by the store
+            tma_store_2d(&tm_hs, box, n, row0);
+            bulk_commit();
           }
         }
       }
@@ -572,6 +577,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1;
       if (acc == 0) aph ^= 1u;
     }
+    // the last boxes' bulk stores are complete (shared memory read, y_perm
+    // and h written) before the CTA leaves
+    if (lane == 0) bulk_wait0();
+    __syncwarp();
   }
 
   pdl_trigger();  // this CTA has no tiles left: the next kernel may launch
@@ -623,7 +632,7 @@ int resident_pairs() {
 
 cudaError_t launch_ffn_tc(const Dims &D, const void *x_perm, int64_t a_rows, const int32_t *offsets, const void *w1,
                           const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
-                          float *y_perm, int32_t *blk_done, int32_t *status, cudaStream_t s) {
+                          void *y_perm, int32_t *blk_done, int32_t *status, cudaStream_t s) {
   if (D.dt != MOE_DT_BF16 || D.N > kMaxExperts || D.d > (1 << 30) || D.d_ff > (1 << 30) || !blk_done)
     return cudaErrorNotSupported;
   static bool attr_set = false;
@@ -646,8 +655,8 @@ cudaError_t launch_ffn_tc(const Dims &D, const void *x_perm, int64_t a_rows, con
   if (pairs < 1) pairs = 1;
   return launch_k(ffn_pair_kernel, dim3(2 * pairs), dim3(kThreads), kSmemP, s, 2u, tx, tw1, th, tw2, ths, offsets,
                   (int)D.N, (int64_t)D.R_max, (int)D.d, (int)D.d_ff, (const __nv_bfloat16 *)b1,
-                  (const __nv_bfloat16 *)b2, row_gate, (__nv_bfloat16 *)h, y_perm, blk_done, (int)ffn_blocks_max(D),
-                  status);
+                  (const __nv_bfloat16 *)b2, row_gate, (__nv_bfloat16 *)h, (__nv_bfloat16 *)y_perm, blk_done,
+                  (int)ffn_blocks_max(D), status);
 }
 
 }  // namespace moe

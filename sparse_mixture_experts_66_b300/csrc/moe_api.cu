@@ -109,7 +109,7 @@ void make_layout(const Dims &D, moe_workspace_layout *L) {
   L->row_gate = take(R * 4);
   L->x_perm = take(R * (size_t)D.d * es);
   L->h = take(R * (size_t)D.d_ff * es);
-  L->y_perm = take(R * (size_t)D.d * 4);
+  L->y_perm = take(R * (size_t)D.d * es);
   const int S = decode_splits(D);
   L->y_split = take(S > 1 ? (size_t)(S - 1) * R * (size_t)D.d * 4 : 0);
   L->ffn_sync = take((size_t)ffn_sync_ints(D) * 4);
@@ -120,7 +120,7 @@ void make_layout(const Dims &D, moe_workspace_layout *L) {
   const Dims S1 = shared_dims(D);
   L->shared_offsets = take(shared ? 8 : 0);
   L->h_shared = take(shared ? (size_t)S1.R_max * (size_t)D.d_ff * es : 0);
-  L->y_shared = take(shared ? (size_t)S1.R_max * (size_t)D.d * 4 : 0);
+  L->y_shared = take(shared ? (size_t)S1.R_max * (size_t)D.d * es : 0);
   L->shared_sync = take(shared ? (size_t)shared_sync_ints(D) * 4 : 0);
   L->total = off;
   L->rows = D.R_max;
@@ -184,7 +184,7 @@ moe_status do_dispatch(const Dims &D, const moe_workspace_layout &L, const void 
 
 moe_status do_ffn(const Dims &D, const moe_workspace_layout &L, const void *x_perm, const int32_t *offsets,
                   const void *w1, const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
-                  float *y_perm, void *ws, cudaStream_t s) {
+                  void *y_perm, void *ws, cudaStream_t s) {
   int32_t *status = AT(ws, L.status, int32_t *);
   if (decode_splits(D) > 0) {
     cudaError_t e = launch_ffn_decode(D, x_perm, offsets, w1, b1, w2, b2, row_gate, h, y_perm,
@@ -209,10 +209,10 @@ moe_status do_ffn(const Dims &D, const moe_workspace_layout &L, const void *x_pe
   return MOE_OK;
 }
 
-moe_status do_combine(const Dims &D, const moe_workspace_layout &L, const float *y_perm, const int32_t *row_of,
+moe_status do_combine(const Dims &D, const moe_workspace_layout &L, const void *y_perm, const int32_t *row_of,
                       const float *gate, const void *x, void *y, void *ws, cudaStream_t s) {
   const int S = decode_splits(D);
-  const float *y_shared = (D.flags & MOE_FLAG_SHARED_EXPERT) ? AT(ws, L.y_shared, const float *) : nullptr;
+  const void *y_shared = (D.flags & MOE_FLAG_SHARED_EXPERT) ? AT(ws, L.y_shared, const void *) : nullptr;
   cudaError_t e = launch_combine(D, y_perm, S > 1 ? AT(ws, L.y_split, const float *) : nullptr, S > 1 ? S - 1 : 0,
                                  row_of, gate, x, y_shared, y, AT(ws, L.status, int32_t *), s);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
@@ -227,7 +227,7 @@ moe_status do_shared(const Dims &D, const moe_workspace_layout &L, const void *x
   int32_t *status = AT(ws, L.status, int32_t *);
   int32_t *offs = AT(ws, L.shared_offsets, int32_t *);
   void *h = AT(ws, L.h_shared, void *);
-  float *y_sh = AT(ws, L.y_shared, float *);
+  void *y_sh = AT(ws, L.y_shared, void *);
   cudaError_t e = launch_shared_setup(offs, S1.R_max, AT(ws, L.shared_sync, int32_t *), shared_sync_ints(D), s);
   if (e != cudaSuccess) return cuda_fail(e, "shared expert setup");
   if (D.dt == MOE_DT_BF16) {
@@ -347,7 +347,7 @@ moe_status moe_dispatch(const moe_config *cfg, const void *x, const int32_t *top
 
 moe_status moe_expert_ffn(const moe_config *cfg, const void *x_perm, const int32_t *offsets, const void *w1,
                           const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
-                          float *y_perm, void *ws, moe_stream_t stream) {
+                          void *y_perm, void *ws, moe_stream_t stream) {
   Dims D;
   TRY(check_config(cfg, &D));
   if (D.flags & MOE_FLAG_EXPERT_CHOICE)
@@ -361,7 +361,7 @@ moe_status moe_expert_ffn(const moe_config *cfg, const void *x_perm, const int32
   return do_ffn(D, L, x_perm, offsets, w1, b1, w2, b2, row_gate, h, y_perm, ws, (cudaStream_t)stream);
 }
 
-moe_status moe_combine(const moe_config *cfg, const float *y_perm, const int32_t *row_of, const float *gate,
+moe_status moe_combine(const moe_config *cfg, const void *y_perm, const int32_t *row_of, const float *gate,
                        const void *x, void *y, void *ws, moe_stream_t stream) {
   Dims D;
   TRY(check_config(cfg, &D));
@@ -407,7 +407,7 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const void *w_g, co
   int32_t *row_of = AT(ws, L.row_of, int32_t *);
   float *row_gate = AT(ws, L.row_gate, float *);
   void *x_perm = AT(ws, L.x_perm, void *);
-  float *y_perm = AT(ws, L.y_perm, float *);
+  void *y_perm = AT(ws, L.y_perm, void *);
   TRY(do_route(D, L, x, w_g, router_bias, topk_idx, gate, score, ws, s));
   if (D.flags & MOE_FLAG_EXPERT_CHOICE) {
     // every token offers itself to every expert (request j of token t goes to
@@ -444,7 +444,7 @@ moe_status moe_forward_shared(const moe_config *cfg, const void *x, const void *
   int32_t *row_of = AT(ws, L.row_of, int32_t *);
   float *row_gate = AT(ws, L.row_gate, float *);
   void *x_perm = AT(ws, L.x_perm, void *);
-  float *y_perm = AT(ws, L.y_perm, float *);
+  void *y_perm = AT(ws, L.y_perm, void *);
   TRY(do_route(D, L, x, w_g, router_bias, topk_idx, gate, score, ws, s));
   TRY(do_dispatch(D, L, x, topk_idx, gate, score, AT(ws, L.counts_raw, int32_t *), AT(ws, L.counts_kept, int32_t *),
                   offsets, row_of, AT(ws, L.row_token, int32_t *), row_gate, x_perm, ws, s));

@@ -193,16 +193,17 @@ inline int row_align(const Dims &D) { return decode_splits(D) > 0 ? kDecodeRowsP
 // (zero on entry, left zero on exit).
 cudaError_t launch_ffn_decode(const Dims &D, const void *x_perm, const int32_t *offsets, const void *w1,
                               const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
-                              float *y_perm, float *y_split, int32_t *h_done, int32_t *status, cudaStream_t s);
+                              void *y_perm, float *y_split, int32_t *h_done, int32_t *status, cudaStream_t s);
 
 cudaError_t launch_permute(const Dims &D, const void *x, const int32_t *offsets, const int32_t *row_token,
                            void *x_perm, int32_t *status, cudaStream_t s);
 
 // y_split / nsplit: the extra K slices of a decode-mode second GEMM (nsplit
 // buffers of [R_max, d] after y_perm's own), added in slice order.
-// y_shared [Tp, d] fp32 or NULL: the shared expert's output, added last.
-cudaError_t launch_combine(const Dims &D, const float *y_perm, const float *y_split, int nsplit,
-                           const int32_t *row_of, const float *gate, const void *x, const float *y_shared, void *y,
+// y_perm and y_shared ([Tp, d] or NULL: the shared expert's output, added
+// last) are in x's dtype; y_split is fp32.
+cudaError_t launch_combine(const Dims &D, const void *y_perm, const float *y_split, int nsplit,
+                           const int32_t *row_of, const float *gate, const void *x, const void *y_shared, void *y,
                            int32_t *status, cudaStream_t s);
 
 // Grouped GEMM over expert segments with the two fused epilogues.
@@ -235,7 +236,7 @@ inline int64_t ffn_sync_ints(const Dims &D) {
 // a_rows: rows of x_perm that exist (TMA zero-fills the rest up to R_max).
 cudaError_t launch_ffn_tc(const Dims &D, const void *x_perm, int64_t a_rows, const int32_t *offsets, const void *w1,
                           const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
-                          float *y_perm, int32_t *blk_done, int32_t *status, cudaStream_t s);
+                          void *y_perm, int32_t *blk_done, int32_t *status, cudaStream_t s);
 
 // Expert-choice requests: idx[t * N + j] = j for every token.
 cudaError_t launch_ec_pattern(int32_t *idx, int64_t T, int N, cudaStream_t s);

@@ -119,21 +119,22 @@ __device__ __forceinline__ void stv(__nv_bfloat16 *p, const float (&v)[W]) {
 // CTA reads the U x KM row indices once and turns them into source-row
 // pointers (null for a dropped pick), so the column loop holds no index
 // arithmetic, and every condition in it is uniform across the CTA. A thread
-// keeps up to U x KM x W / 4 16-byte loads in flight. The picks of a token are
-// added in pick order.
+// keeps one 16-byte load per source row in flight (y_perm is in x's dtype: 8
+// bf16 or 4 fp32 columns). The picks of a token are added, as fp32, in pick
+// order, and the sum is rounded once to x's dtype.
 constexpr int kC8Threads = 128;
 template <typename T, int KM, int W>
-__global__ void __launch_bounds__(kC8Threads) combine_kernel(const float *__restrict__ y_perm, int64_t d,
+__global__ void __launch_bounds__(kC8Threads) combine_kernel(const T *__restrict__ y_perm, int64_t d,
                                                              const int32_t *__restrict__ row_of,
                                                              const float *__restrict__ gate,
                                                              const T *__restrict__ x,
-                                                             const float *__restrict__ y_shared, int64_t T_, int k,
+                                                             const T *__restrict__ y_shared, int64_t T_, int k,
                                                              int64_t R_max, uint32_t flags, T *__restrict__ y,
                                                              int32_t *status) {
   pdl_wait();
   constexpr int U = 8 / KM;
   const int64_t t0 = (int64_t)blockIdx.x * U;
-  const float *src[U][KM];  // source row of each kept pick, or null
+  const T *src[U][KM];  // source row of each kept pick, or null
   float ksum[U];            // kept-gate sum (for MOE_FLAG_RENORM_SURVIVORS)
   bool live[U], renorm[U], ident[U];
 #pragma unroll
@@ -201,10 +202,11 @@ __global__ void __launch_bounds__(kC8Threads) combine_kernel(const float *__rest
 // Combine of many picks per token (k > 8: expert-choice routing, where every
 // expert may take a token): a CTA owns one token, threads stride its columns;
 // the picks are walked in order and most are -1. No flag variants apply.
-__global__ void __launch_bounds__(kCombineThreads) combine_many_kernel(const float *__restrict__ y_perm, int64_t d,
+template <typename T>
+__global__ void __launch_bounds__(kCombineThreads) combine_many_kernel(const T *__restrict__ y_perm, int64_t d,
                                                                        const int32_t *__restrict__ row_of, int k,
-                                                                       int64_t R_max, int64_t T_, void *y_out,
-                                                                       int bf16, int32_t *status) {
+                                                                       int64_t R_max, int64_t T_, T *__restrict__ y,
+                                                                       int32_t *status) {
   pdl_wait();
   const int64_t t = blockIdx.x;
   if (t >= T_) return;
@@ -217,14 +219,13 @@ __global__ void __launch_bounds__(kCombineThreads) combine_many_kernel(const flo
         if (c == 0) report_error(status, MOE_ERR_BOUNDS, kKCombine, (int32_t)t);
         continue;
       }
-      const float4 v = __ldg(reinterpret_cast<const float4 *>(y_perm + (int64_t)r * d + c));
+      const float4 v = Store4<T>::ld(y_perm + (int64_t)r * d + c);
       a.x += v.x;
       a.y += v.y;
       a.z += v.z;
       a.w += v.w;
     }
-    if (bf16) Store4<__nv_bfloat16>::st(reinterpret_cast<__nv_bfloat16 *>(y_out) + t * d + c, a);
-    else Store4<float>::st(reinterpret_cast<float *>(y_out) + t * d + c, a);
+    Store4<T>::st(y + t * d + c, a);
   }
 }
 
@@ -241,9 +242,9 @@ __global__ void ec_pattern_kernel(int32_t *idx, int64_t T_, int N) {
 // the picks in pick order.
 template <typename T>
 __global__ void __launch_bounds__(kCombineThreads) combine_split_kernel(
-    const float *__restrict__ y_perm, const float *__restrict__ y_split, int nsplit, int64_t d,
+    const T *__restrict__ y_perm, const float *__restrict__ y_split, int nsplit, int64_t d,
     const int32_t *__restrict__ row_of, const float *__restrict__ gate, const T *__restrict__ x,
-    const float *__restrict__ y_shared, int64_t T_, int k, int64_t R_max, uint32_t flags, T *__restrict__ y,
+    const T *__restrict__ y_shared, int64_t T_, int k, int64_t R_max, uint32_t flags, T *__restrict__ y,
     int32_t *status) {
   pdl_wait();
   const int64_t d4 = d >> 2;
@@ -270,16 +271,16 @@ __global__ void __launch_bounds__(kCombineThreads) combine_split_kernel(
     for (int b = 0; b < 8; ++b) {
       const int q = q0 + b;
       const int j = q / per, sl = q - j * per;
-      const float *src = y_perm;
       int64_t r = 0;
       ok[b] = false;
       if (q < nsrc) {
         const int32_t rr = __ldg(row_of + t * k + j);
         ok[b] = rr >= 0 && rr < R_max;
         r = ok[b] ? rr : 0;
-        if (sl > 0) src = y_split + (int64_t)(sl - 1) * R_max * d;
       }
-      v[b] = __ldg(reinterpret_cast<const float4 *>(src + r * d + c));
+      // slice 0 in y_perm (x's dtype), the others in y_split (fp32)
+      v[b] = sl == 0 ? Store4<T>::ld(y_perm + r * d + c)
+                     : __ldg(reinterpret_cast<const float4 *>(y_split + (int64_t)(sl - 1) * R_max * d + r * d + c));
     }
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
@@ -310,7 +311,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_split_kernel(
   }
   if ((flags & MOE_FLAG_IDENTITY_FALLBACK) && nkept == 0) acc = Store4<T>::ld(x + t * d + c);
   if (y_shared) {  // the shared expert, added last
-    const float4 sh = __ldg(reinterpret_cast<const float4 *>(y_shared + t * d + c));
+    const float4 sh = Store4<T>::ld(y_shared + t * d + c);
     acc.x += sh.x;
     acc.y += sh.y;
     acc.z += sh.z;
@@ -339,8 +340,8 @@ cudaError_t launch_permute(const Dims &D, const void *x, const int32_t *offsets,
 
 namespace {
 template <typename T>
-cudaError_t launch_combine_t(const Dims &D, const float *y_perm, const float *y_split, int nsplit,
-                             const int32_t *row_of, const float *gate, const T *x, const float *y_shared, T *y,
+cudaError_t launch_combine_t(const Dims &D, const T *y_perm, const float *y_split, int nsplit,
+                             const int32_t *row_of, const float *gate, const T *x, const T *y_shared, T *y,
                              int32_t *status, cudaStream_t s) {
   const int64_t items = D.T * (D.d / 4);
   if (nsplit > 0) {
@@ -363,22 +364,26 @@ cudaError_t launch_combine_t(const Dims &D, const float *y_perm, const float *y_
 }
 }  // namespace
 
-cudaError_t launch_combine(const Dims &D, const float *y_perm, const float *y_split, int nsplit,
-                           const int32_t *row_of, const float *gate, const void *x, const float *y_shared, void *y,
+cudaError_t launch_combine(const Dims &D, const void *y_perm, const float *y_split, int nsplit,
+                           const int32_t *row_of, const float *gate, const void *x, const void *y_shared, void *y,
                            int32_t *status, cudaStream_t s) {
   if (!y_split) nsplit = 0;
   if (nsplit > 7) return cudaErrorNotSupported;
   if (D.T == 0) return cudaSuccess;
   if (D.k > 8 && nsplit == 0) {
     if (y_shared || (D.flags & (MOE_FLAG_RENORM_SURVIVORS | MOE_FLAG_IDENTITY_FALLBACK))) return cudaErrorNotSupported;
-    return launch_k(combine_many_kernel, dim3((unsigned)D.T), dim3(kCombineThreads), 0, s, 1u, y_perm, D.d, row_of,
-                    D.k, D.R_max, D.T, y, D.dt == MOE_DT_BF16 ? 1 : 0, status);
+    if (D.dt == MOE_DT_BF16)
+      return launch_k(combine_many_kernel<__nv_bfloat16>, dim3((unsigned)D.T), dim3(kCombineThreads), 0, s, 1u,
+                      (const __nv_bfloat16 *)y_perm, D.d, row_of, D.k, D.R_max, D.T, (__nv_bfloat16 *)y, status);
+    return launch_k(combine_many_kernel<float>, dim3((unsigned)D.T), dim3(kCombineThreads), 0, s, 1u,
+                    (const float *)y_perm, D.d, row_of, D.k, D.R_max, D.T, (float *)y, status);
   }
   if (D.dt == MOE_DT_BF16)
-    return launch_combine_t<__nv_bfloat16>(D, y_perm, y_split, nsplit, row_of, gate, (const __nv_bfloat16 *)x,
-                                           y_shared, (__nv_bfloat16 *)y, status, s);
-  return launch_combine_t<float>(D, y_perm, y_split, nsplit, row_of, gate, (const float *)x, y_shared, (float *)y,
-                                 status, s);
+    return launch_combine_t<__nv_bfloat16>(D, (const __nv_bfloat16 *)y_perm, y_split, nsplit, row_of, gate,
+                                           (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)y_shared,
+                                           (__nv_bfloat16 *)y, status, s);
+  return launch_combine_t<float>(D, (const float *)y_perm, y_split, nsplit, row_of, gate, (const float *)x,
+                                 (const float *)y_shared, (float *)y, status, s);
 }
 
 namespace {

@@ -260,13 +260,13 @@ class Workspace:
             offsets=self.view("offsets", torch.int32, (N + 1,)), row_of=self.view("row_of", torch.int32, (T, k)),
             row_token=self.view("row_token", torch.int32, (R,)), row_gate=self.view("row_gate", torch.float32, (R,)),
             x_perm=self.view("x_perm", dt, (R, c.d)), h=self.view("h", dt, (R, c.d_ff)),
-            y_perm=self.view("y_perm", torch.float32, (R, c.d)),
+            y_perm=self.view("y_perm", dt, (R, c.d)),
             y_split=self.view("y_split", torch.float32, (self.splits - 1, R, c.d)),
             probs=self.view("probs", torch.float32,
                             (T, N) if c.flags & (MOE_FLAG_ROUTER_STATS | MOE_FLAG_EXPERT_CHOICE) else (0, N)),
             lse=self.view("lse", torch.float32,
                           (T,) if c.flags & (MOE_FLAG_ROUTER_STATS | MOE_FLAG_EXPERT_CHOICE) else (0,)),
-            y_shared=self.view("y_shared", torch.float32,
+            y_shared=self.view("y_shared", dt,
                                ((T + 127) // 128 * 128, c.d) if c.flags & MOE_FLAG_SHARED_EXPERT else (0, c.d)))
 
     @property

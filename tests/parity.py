@@ -47,7 +47,7 @@ def run_gpu(w, inp, flags=0, dev=None, reps=1):
     ws.status()
     v = ws.views()
     out = {k: t.cpu() for k, t in v.items() if k not in ("x_perm", "h", "y_perm", "y_split")}
-    out = {k: t.numpy() for k, t in out.items()}
+    out = {k: (t.float() if t.dtype == torch.bfloat16 else t).numpy() for k, t in out.items()}
     out["y"] = y.float().cpu().numpy().astype(np.float64)
     out["_ws"], out["_cfg"], out["_dev"], out["_y"] = ws, cfg, dev, y
     return out

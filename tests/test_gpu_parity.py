@@ -71,12 +71,13 @@ def test_permute_is_an_exact_gather(w):
 @pytest.mark.parametrize("w", STAGE_CASES[:3] + [custom(64, 1024, 4096, 8, 2, math.inf, seed=13)],
                          ids=lambda w: w.name)
 def test_combine_is_the_fixed_order_fp32_sum(w):
-    """y[t] = sum over kept picks in pick order of y_perm rows, in fp32, then
-    rounded once to the storage dtype: reproduced bit for bit."""
+    """y[t] = sum over kept picks in pick order of y_perm rows (x's dtype,
+    widened exactly), in fp32, then rounded once to the storage dtype:
+    reproduced bit for bit."""
     inp = draw(w)
     g = parity.run_gpu(w, inp)
     v = g["_ws"].views()
-    yp = v["y_perm"].cpu().numpy()
+    yp = v["y_perm"].float().cpu().numpy()
     ys = v["y_split"].cpu().numpy()
     acc = np.zeros((w.T, w.d), dtype=np.float32)
     for j in range(w.k):
@@ -97,7 +98,7 @@ def test_expert_ffn_rows_against_oracle(w):
     g = parity.run_gpu(w, inp)
     v = g["_ws"].views()
     xp = v["x_perm"].float().cpu().numpy()
-    yp = v["y_perm"].cpu().numpy()
+    yp = v["y_perm"].float().cpu().numpy()
     off = g["offsets"]
     w1, b1, w2, b2 = (as_f32_numpy(inp[n]) for n in ("w1", "b1", "w2", "b2"))
     rng = np.random.default_rng(0)
@@ -230,7 +231,7 @@ def test_stage_calls_compose_to_forward():
     moe.moe_dispatch(cfg, dev["x"], topk_idx, gate, score, counts_raw, counts_kept, offsets, row_of, row_token,
                      row_gate, x_perm, ws.buf)
     h = torch.empty(R, w.d_ff, dtype=dev["x"].dtype, device="cuda")
-    y_perm = torch.empty(R, w.d, **f32)
+    y_perm = torch.empty(R, w.d, dtype=dev["x"].dtype, device="cuda")
     moe.moe_expert_ffn(cfg, x_perm, offsets, dev["w1"], dev["b1"], dev["w2"], dev["b2"], row_gate, h, y_perm, ws.buf)
     y = torch.empty_like(dev["x"])
     moe.moe_combine(cfg, y_perm, row_of, gate, dev["x"], y, ws.buf)
@@ -429,9 +430,9 @@ def test_expert_ffn_accepts_16_byte_aligned_outputs():
     v = ws.views()
     R = ws.layout.rows
     hb = torch.empty(R * w.d_ff * 2 + 32, dtype=torch.uint8, device="cuda")
-    yb = torch.empty(R * w.d * 4 + 32, dtype=torch.uint8, device="cuda")
+    yb = torch.empty(R * w.d * 2 + 32, dtype=torch.uint8, device="cuda")
     h16 = hb[16:16 + R * w.d_ff * 2].view(torch.bfloat16).view(R, w.d_ff)
-    y16 = yb[16:16 + R * w.d * 4].view(torch.float32).view(R, w.d)
+    y16 = yb[16:16 + R * w.d * 2].view(torch.bfloat16).view(R, w.d)
     d = g["_dev"]
     moe.moe_expert_ffn(cfg, v["x_perm"], v["offsets"], d["w1"], d["b1"], d["w2"], d["b2"], v["row_gate"], h16, y16,
                        ws.buf)
