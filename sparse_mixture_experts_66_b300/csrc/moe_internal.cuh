@@ -115,30 +115,28 @@ __device__ __forceinline__ float gelu_as(float u) {
   return u >= 0.f ? u * fmaf(-0.5f, q, 1.0f) : 0.5f * u * q;
 }
 
-// gelu_as on two values at once: the same formula, with the multiply-adds on
-// the packed two-lane fp32 units (one instruction per pair) and the
-// reciprocal and exp2 per value. For u >= 0 the result is formed as
-// u - u q/2 with one rounding.
+// gelu_as on two values at once, with the multiply-adds on the packed
+// two-lane fp32 units (one instruction per pair) and the reciprocal and exp2
+// per value. Same erf (A&S 7.1.26, x = |u|/sqrt 2), arranged to need no sign
+// select and no cancellation: GELU(u) = max(u, 0) - |u| erfc(x)/2, with
+// erfc(x)/2 = (sum of a_i t^i)/2 * exp(-x^2); the factor -1/2 is folded into
+// the coefficients, 1/sqrt 2 into p and into the exponent (-u^2/2, base 2).
 __device__ __forceinline__ float2 gelu_as2(float2 u) {
-  const float2 z = __fmul2_rn(make_float2(fabsf(u.x), fabsf(u.y)),
-                              make_float2(0.70710678118654752440f, 0.70710678118654752440f));
-  const float2 den = __ffma2_rn(make_float2(0.3275911f, 0.3275911f), z, make_float2(1.0f, 1.0f));
+  const float2 au = make_float2(fabsf(u.x), fabsf(u.y));
+  const float2 den = __ffma2_rn(make_float2(0.23164188826636f, 0.23164188826636f), au, make_float2(1.0f, 1.0f));
   float2 t;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t.x) : "f"(den.x));
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t.y) : "f"(den.y));
-  float2 p = __ffma2_rn(t, make_float2(1.061405429f, 1.061405429f), make_float2(-1.453152027f, -1.453152027f));
-  p = __ffma2_rn(t, p, make_float2(1.421413741f, 1.421413741f));
-  p = __ffma2_rn(t, p, make_float2(-0.284496736f, -0.284496736f));
-  p = __ffma2_rn(t, p, make_float2(0.254829592f, 0.254829592f));
-  p = __fmul2_rn(t, p);
-  const float2 arg = __fmul2_rn(__fmul2_rn(z, z), make_float2(-1.44269504088896341f, -1.44269504088896341f));
+  float2 p = __ffma2_rn(t, make_float2(-0.5307027145f, -0.5307027145f), make_float2(0.7265760135f, 0.7265760135f));
+  p = __ffma2_rn(t, p, make_float2(-0.7107068705f, -0.7107068705f));
+  p = __ffma2_rn(t, p, make_float2(0.142248368f, 0.142248368f));
+  p = __ffma2_rn(t, p, make_float2(-0.127414796f, -0.127414796f));
+  p = __fmul2_rn(t, p);  // -(sum of a_i t^i)/2
+  const float2 arg = __fmul2_rn(__fmul2_rn(u, u), make_float2(-0.72134752044448170f, -0.72134752044448170f));
   float2 e;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e.x) : "f"(arg.x));
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e.y) : "f"(arg.y));
-  const float2 hq = __fmul2_rn(__fmul2_rn(p, e), make_float2(0.5f, 0.5f));  // erfc(|u|/sqrt 2) / 2
-  const float2 neg = __fmul2_rn(u, hq);
-  const float2 pos = __ffma2_rn(make_float2(-u.x, -u.y), hq, u);
-  return make_float2(u.x >= 0.f ? pos.x : neg.x, u.y >= 0.f ? pos.y : neg.y);
+  return __ffma2_rn(au, __fmul2_rn(p, e), make_float2(fmaxf(u.x, 0.f), fmaxf(u.y, 0.f)));  // relu(u) - |u| erfc/2
 }
 
 // The expert whose segment holds row r: offsets is non-decreasing, N+1 long.
