@@ -254,7 +254,7 @@ const char *moe_version(void) { return "sparse-moe-b300 0.1 (sm_103a)"; }
 const char *moe_last_error(void) { return g_err; }
 
 int64_t moe_capacity(const moe_config *cfg) {
-  Dims D;
+  Dims D{};
   if (check_config(cfg, &D) != MOE_OK) return -1;
   return D.C;
 }
