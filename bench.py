@@ -3,7 +3,9 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
 One step = one full layer forward (router, capacity + dispatch, expert FFNs,
-combine) over one batch of the workload, inputs resident in HBM. The step is
+combine) over one batch of the workload, inputs resident in HBM. The default
+workload is the largest single-GPU one: the bf16 prefill shape T=16384,
+d=4096, N=8, k=2, d_ff=14336 with no capacity limit. The step is
 issued as the four stage calls of the C ABI (moe_route, moe_dispatch,
 moe_expert_ffn, moe_combine: exactly the launches moe_forward makes). The
 value's timed region records CUDA events at the step boundaries only, on the
@@ -12,12 +14,14 @@ the expert FFN launch for its roofline, and a third pass with an event after
 every stage gives the stage breakdown. Between timed steps L2 is flushed (a
 512 MiB write, then a 1 GiB read, outside the events) unless a step streams at
 least twice the L2 size, in which case its inputs are larger than L2. ``e2e`` times
-moe_forward with the batch copied from pinned host memory and the output
-copied back inside each step.
+moe_forward with each step's batch copied in from pinned host memory and its
+output copied back inside the timed region, the copies of neighbouring steps
+overlapping the forward on a second stream (double-buffered x and y).
 
 Multi-GPU: replicas only (capacity couples every token of a batch, so a batch
 is not split); every rank runs its own batch and value = all tokens / the
-slowest rank's time. Prints one JSON line on rank 0.
+slowest rank's time. ``--gpus N`` without a launcher re-runs this script under
+torch.distributed.run with N ranks. Prints one JSON line on rank 0.
 """
 from __future__ import annotations
 
@@ -38,7 +42,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from sparse_mixture_experts_66_b300 import moe  # noqa: E402
-from sparse_mixture_experts_66_b300.workload import HEADLINE, WORKLOADS, as_f32_numpy, draw  # noqa: E402
+from sparse_mixture_experts_66_b300.workload import PREFILL, WORKLOADS, as_f32_numpy, draw  # noqa: E402
 
 METRIC = "MoE-layer fwd tokens/s on 1 B300; % of bf16 tensor / HBM roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
@@ -215,6 +219,26 @@ class Stages:
         self.combine(s)
 
 
+def l2_policy(w, streamed_bytes):
+    """Whether timed steps flush L2, and the sentence that says so: a step that
+    streams at least twice the L2 size has inputs larger than L2; otherwise a
+    512 MiB write and a 1 GiB read evict L2 between timed steps."""
+    use_flush = streamed_bytes < 2 * L2_BYTES
+    note = ("flushed between timed steps outside the events (512 MiB write, then 1 GiB read)" if use_flush else
+            f"inputs larger than L2: {streamed_bytes / 1e9:.2f} GB streamed per step, "
+            f"{streamed_bytes / L2_BYTES:.0f}x the 126 MB L2; no flush")
+    return use_flush, note
+
+
+def config_dict(w, capacity, counts_kept, world):
+    """The workload as both arms report it (the same dict in both lines)."""
+    alg = algorithmic(w, counts_kept)
+    return {"workload": w.name, "T": w.T, "d": w.d, "N": w.N, "k": w.k, "d_ff": w.d_ff,
+            "capacity_factor": None if math.isinf(w.capacity_factor) else w.capacity_factor,
+            "router_bias": w.router_bias, "capacity": int(capacity), "kept_rows": alg["R"],
+            "active_experts": alg["A"], "parallelism": f"replicas{world}", "l2": l2_policy(w, alg["bytes"])[1]}
+
+
 def algorithmic(w, counts_kept):
     """Algorithmic FLOPs and bytes of one forward (kept rows only; padding and
     intermediates excluded)."""
@@ -239,15 +263,18 @@ def run_ours(args, world, rank, local):
     ws = moe.Workspace(cfg, device=device)
     st = Stages(cfg, dev, ws)
     stream = torch.cuda.current_stream(device)
-    flush_w = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)
-    flush_r = torch.empty(256 * 1024 * 1024, dtype=torch.float32, device=device)
+    flush_bufs = []
 
     def flush():
         """Evict L2: write 512 MiB, then read 1 GiB, so that L2 holds none of
         the step's data and no dirty lines whose write-back would land in the
-        next step."""
-        flush_w.zero_()
-        flush_r.sum()
+        next step. (The buffers are allocated on first use: workloads whose
+        steps stream more than twice the L2 size never flush.)"""
+        if not flush_bufs:
+            flush_bufs.append(torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device))
+            flush_bufs.append(torch.zeros(256 * 1024 * 1024, dtype=torch.float32, device=device))
+        flush_bufs[0].zero_()
+        flush_bufs[1].sum()
 
     for _ in range(max(args.warmup, 3)):
         st.all(stream)
@@ -258,11 +285,7 @@ def run_ours(args, world, rank, local):
     # L2 between timed steps: when a step streams at least twice the L2 size
     # (the weights of the active experts), its inputs are larger than L2 and
     # no flush is needed; otherwise a 512 MiB write evicts L2 before each step.
-    streamed = alg["bytes"]
-    use_flush = streamed < 2 * L2_BYTES
-    l2_note = ("flushed between timed steps outside the events (512 MiB write, then 1 GiB read)" if use_flush else
-               f"inputs larger than L2: {streamed / 1e9:.2f} GB streamed per step, {streamed / L2_BYTES:.0f}x "
-               "the 126 MB L2; no flush")
+    use_flush, _ = l2_policy(w, alg["bytes"])
 
     K = args.steps
     # Timed region 1 (the value): events at the step boundaries only, so the
@@ -326,32 +349,74 @@ def run_ours(args, world, rank, local):
     value, slowest_s = aggregate_throughput(w.T, ms * 1e-3, world, device)
     ms_max = slowest_s * 1e3
 
-    # end to end through moe_forward with host buffers
+    # End to end through moe_forward with host buffers: every step copies its
+    # batch in from pinned host memory and its output back, inside the timed
+    # region. When the workload needs no L2 flush the steps are pipelined: x of
+    # step i+1 is copied in (copy stream) and y of step i-1 copied out (a second
+    # copy stream) while step i computes, with x and y double-buffered on the
+    # device. Workloads timed with L2 flushes run the copies and the forward
+    # serially, each step between its own events with the flush outside them.
     x_host = inp["x"].pin_memory()
-    y_host = torch.empty_like(x_host).pin_memory()
-    x_dev = torch.empty_like(dev["x"])
-    y_dev = torch.empty_like(dev["x"])
-    for _ in range(3):
-        x_dev.copy_(x_host, non_blocking=True)
-        moe.moe_forward(cfg, x_dev, dev["w_g"], dev["router_bias"], dev["w1"], dev["b1"], dev["w2"], dev["b2"],
-                        y_dev, ws.buf, stream)
-        y_host.copy_(y_dev, non_blocking=True)
+    y_host = [torch.empty_like(x_host).pin_memory() for _ in range(2)]
+    x_dev = [torch.empty_like(dev["x"]) for _ in range(2)]
+    y_dev = [torch.empty_like(dev["x"]) for _ in range(2)]
+
+    def fwd(xd, yd):
+        moe.moe_forward(cfg, xd, dev["w_g"], dev["router_bias"], dev["w1"], dev["b1"], dev["w2"], dev["b2"], yd,
+                        ws.buf, stream)
+
+    for i in range(3):
+        x_dev[0].copy_(x_host, non_blocking=True)
+        fwd(x_dev[0], y_dev[0])
+        y_host[0].copy_(y_dev[0], non_blocking=True)
     torch.cuda.synchronize(device)
-    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     barrier(world)
-    for i in range(K):
-        if use_flush:
+    if use_flush:
+        e2e_mode = "serial: copy in, forward, copy out per step; L2 flushed between steps outside the events"
+        e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for i in range(K):
             flush()
-        e2e_ev[i][0].record(stream)
-        x_dev.copy_(x_host, non_blocking=True)
-        moe.moe_forward(cfg, x_dev, dev["w_g"], dev["router_bias"], dev["w1"], dev["b1"], dev["w2"], dev["b2"],
-                        y_dev, ws.buf, stream)
-        y_host.copy_(y_dev, non_blocking=True)
-        e2e_ev[i][1].record(stream)
-    torch.cuda.synchronize(device)
+            e2e_ev[i][0].record(stream)
+            x_dev[0].copy_(x_host, non_blocking=True)
+            fwd(x_dev[0], y_dev[0])
+            y_host[0].copy_(y_dev[0], non_blocking=True)
+            e2e_ev[i][1].record(stream)
+        torch.cuda.synchronize(device)
+        e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)
+    else:
+        e2e_mode = ("pipelined: step i+1's x copied in and step i-1's y copied out on two copy streams while step "
+                    "i computes (x, y double-buffered); one event pair around all K steps")
+        s_in = torch.cuda.Stream(device)
+        s_out = torch.cuda.Stream(device)
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        in_done = [ev() for _ in range(K)]
+        fwd_done = [ev() for _ in range(K)]
+        out_done = [ev() for _ in range(K)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        s_in.wait_event(t0)
+        s_out.wait_event(t0)
+        for i in range(K):
+            b = i % 2
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(fwd_done[i - 2])  # the forward of step i-2 has read x_dev[b]
+                x_dev[b].copy_(x_host, non_blocking=True)
+                in_done[i].record(s_in)
+            stream.wait_event(in_done[i])
+            if i >= 2:
+                stream.wait_event(out_done[i - 2])  # y_dev[b] of step i-2 is back on the host
+            fwd(x_dev[b], y_dev[b])
+            fwd_done[i].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(fwd_done[i])
+                y_host[b].copy_(y_dev[b], non_blocking=True)
+                out_done[i].record(s_out)
+        t1.record(s_out)
+        torch.cuda.synchronize(device)
+        e2e_ms = t0.elapsed_time(t1) / K
     barrier(world)
     ws.status(stream)
-    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)
     e2e_value, _ = aggregate_throughput(w.T, e2e_ms * 1e-3, world, device)
     es = 2 if w.dtype == "bf16" else 4
 
@@ -384,11 +449,7 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic: seeded normal draws (torch CPU generator, seed 0), fan-in scaled weights",
-        "config": {"workload": w.name, "T": w.T, "d": w.d, "N": w.N, "k": w.k, "d_ff": w.d_ff,
-                   "capacity_factor": None if math.isinf(w.capacity_factor) else w.capacity_factor,
-                   "router_bias": w.router_bias, "capacity": ws.layout.capacity, "kept_rows": alg["R"],
-                   "active_experts": alg["A"], "parallelism": f"replicas{world}",
-                   "l2": l2_note},
+        "config": config_dict(w, ws.layout.capacity, counts_kept, world),
         "roofline": roof,
         "step": {"tflops": step_flops, "gbs": step_gbs,
                  "frac_tensor_roofline": (alg["flops"] / (peaks["bf16_tflops"] * 1e12)) / (ms * 1e-3),
@@ -396,7 +457,7 @@ def run_ours(args, world, rank, local):
                  "stages_ms": stage_ms, "ms_min": min(step_ms), "ms_median": statistics.median(step_ms),
                  "wall_s": t_wall},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": w.T * w.d * es,
-                "d2h_bytes_per_step": w.T * w.d * es, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": w.T * w.d * es, "ms_per_step": e2e_ms, "mode": e2e_mode},
         "gpu_launches": kernels_per_step(w) * K,
         "clocks": clk,
     }
@@ -449,7 +510,13 @@ def cpu_baseline(w, inp, budget_s=15.0):
 
 
 def run_reference(args, world, rank):
-    """The oracle timed on the host cores as the reference arm."""
+    """The oracle timed on the host cores as the reference arm, on the same
+    workload and config as the GPU arm. A step runs the whole batch when that
+    fits the per-step budget (--ref-budget over warm-up plus timed steps);
+    otherwise routing and capacity of the whole batch plus the expert FFNs and
+    combine of the first n tokens (a bounded sample), and the tokens/s value is
+    extrapolated to the whole batch. ms_per_step is the measured time of the
+    steps actually run, so ms_per_step x steps is the time spent timing."""
     w = WORKLOADS[args.workload]
     inp = draw(w)
     import oracle
@@ -458,24 +525,45 @@ def run_reference(args, world, rank):
     arrays, rb = _oracle_inputs(inp)
     steps = args.steps + args.warmup
     fixed, per_tok, _ = _oracle_costs(orc, w, arrays, rb, 1e9)
-    per_step_budget = max(args.ref_budget / steps, fixed + per_tok)
-    n = int(max(1, min(w.T, (per_step_budget - fixed) / per_tok)))
+    per_step_budget = args.ref_budget / max(steps, 1)
+    full = fixed + per_tok * w.T <= per_step_budget
+    n = w.T if full else int(max(1, min(w.T, (per_step_budget - fixed) / per_tok)))
     for _ in range(args.warmup):
         _oracle_step(orc, w, arrays, rb, n)
     ts = [_oracle_step(orc, w, arrays, rb, n) for _ in range(args.steps)]
     t = statistics.mean(ts)
-    est = fixed + max(t - fixed, 1e-9) / n * w.T
+    est = t if full else fixed + max(t - fixed, 1e-9) / n * w.T
     value = w.T / est
+    ref0 = orc.forward(*arrays, k=w.k, cf=w.capacity_factor, router_bias=rb, sel=np.arange(0, dtype=np.int64))
     cores = int(os.environ.get("OMP_NUM_THREADS", len(os.sched_getaffinity(0))))
-    sample = (f"each step: routing+capacity over all {w.T} tokens and expert FFNs+combine for {n} of {w.T} "
-              f"tokens (fp64 CPU oracle); tokens/s extrapolated to the whole batch")
+    if full:
+        sample = f"each step: the whole batch of {w.T} tokens (fp64 CPU oracle)"
+    else:
+        sample = (f"each step: routing+capacity over all {w.T} tokens and expert FFNs+combine for {n} of {w.T} "
+                  f"tokens (fp64 CPU oracle, {t:.2f} s measured per step); tokens/s extrapolated to the whole "
+                  f"batch ({est:.1f} s per full step)")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": est * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (same draws as ours)",
-            "config": {"workload": w.name, "T": w.T, "d": w.d, "N": w.N, "k": w.k, "d_ff": w.d_ff,
-                       "parallelism": "host cores"},
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic: seeded normal draws (torch CPU generator, seed 0), fan-in scaled weights",
+            "config": config_dict(w, ref0["C"], ref0["counts_kept"], world),
+            "timed_region_s": t * args.steps, "tokens_per_timed_step": n, "extrapolated": not full,
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
-            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "note": "host-core arm: no L2 flush applies; the config's l2 entry describes the GPU arm"}
+
+
+def relaunch(n):
+    """Re-run this script under torch.distributed.run with n ranks on this
+    node (one per GPU), passing the same arguments; returns its exit code."""
+    import socket
+
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", f"--master-port={port}", os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
 
 
 def main():
@@ -483,12 +571,14 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=PREFILL, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=90.0)
     args = ap.parse_args()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(relaunch(args.gpus))
     world, rank, local = dist_info()
     if args.impl == "reference":
         if rank != 0:

@@ -287,6 +287,23 @@ moe_status moe_forward_noalloc(const moe_config *cfg, const void *x, const void 
                                const void *w1, const void *b1, const void *w2, const void *b2, void *y,
                                moe_stream_t stream);
 
+/* Self-test of the library's failure handling (the pages have no counterpart:
+ * this checks a property of the library, not of the method). Every wait inside
+ * the pipelined kernels, on an mbarrier phase or on a completion counter that
+ * another CTA raises, is bounded: when its limit passes, the kernel records
+ * MOE_ERR_TIMEOUT in the workspace's status word and leaves cleanly. This call
+ * launches one CTA that runs those same two wait routines on a barrier that
+ * nothing arms and on a counter that nothing raises, each for limit_ns
+ * nanoseconds (1000 .. 10^9), so that a test can watch both give up.
+ *   ws: any workspace (only its 64-byte status word, at offset 0, is used;
+ *   moe_get_device_status then returns MOE_ERR_TIMEOUT until moe_workspace_init
+ *   clears it). result: device int32[8], 16-byte aligned: [0] and [1] are 1 if
+ *   the barrier / counter wait succeeded (0 is expected), [2] and [3] the
+ *   microseconds each wait lasted, [4] the counter (cleared here before the
+ *   launch). MOE_ERR_INVALID_ARG for a limit outside the range or a bad
+ *   pointer. */
+moe_status moe_selftest_wait_timeout(void *ws, int64_t limit_ns, int32_t *result, moe_stream_t stream);
+
 #if defined(__GNUC__)
 #pragma GCC visibility pop
 #endif

@@ -148,14 +148,31 @@ __global__ void __launch_bounds__(kThreads) capacity_kernel(
   const int64_t off = s_off;
   const int count = s_count;
   const int kept_e = (int64_t)count < C ? count : (int)C;
+  if (total_rows > R_max) {
+    // Cannot happen for consistent inputs (R_max bounds every padded
+    // segment). Leave an empty, well-formed dispatch rather than rows of an
+    // earlier call: no kept rows, every request of this expert dropped.
+    if (threadIdx.x == 0) {
+      counts_raw[e] = count;
+      counts_kept[e] = 0;
+      offsets[e] = 0;
+      if (e == N - 1) offsets[N] = 0;
+      report_error(status, MOE_ERR_BOUNDS, kKCapAssign, e);
+    }
+    for (int64_t base = 0; base < n; base += kChunk) {
+      if (!kResident) load_items(idx, score, gate, n, base + my0, it);
+#pragma unroll
+      for (int q = 0; q < kItems; ++q)
+        if (it.ie[q] == e) row_of[base + my0 + q] = -1;
+    }
+    return;
+  }
   if (threadIdx.x == 0) {
     counts_raw[e] = count;
     counts_kept[e] = kept_e;
     offsets[e] = (int32_t)off;
     if (e == N - 1) offsets[N] = total_rows;
-    if (total_rows > R_max) report_error(status, MOE_ERR_BOUNDS, kKCapAssign, e);
   }
-  if (total_rows > R_max) return;  // cannot happen for consistent inputs
 
   // 2. the C-th largest score of this expert, when it overflows
   const bool overflow = (int64_t)count > C;

@@ -442,12 +442,15 @@ cudaError_t launch_ffn_decode(const Dims &D, const void *x_perm, const int32_t *
                               void *y_perm, float *y_split, int32_t *h_done, int32_t *status, cudaStream_t s) {
   const int S = decode_splits(D);
   if (S < 1 || (S > 1 && !y_split) || !h_done || D.N > kDMaxExperts) return cudaErrorNotSupported;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(ffn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static PerDevice<int> attr;  // the kernel's shared-memory size, set once per device
+  int set = 0;
+  const cudaError_t ae = attr.get(
+      [](int *v) {
+        *v = 1;
+        return cudaFuncSetAttribute(ffn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDSmem);
+      },
+      &set);
+  if (ae != cudaSuccess) return ae;
   CUtensorMap tw1, tx, tw2, th;
   const uint64_t dw1[3] = {(uint64_t)D.d, (uint64_t)D.d_ff, (uint64_t)D.N};
   const uint64_t dx[2] = {(uint64_t)D.d, (uint64_t)D.R_max};

@@ -602,30 +602,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Clusters of 2 that can be resident at once (every pair must be, for the
-// GEMM2 tiles' waits to end).
-int resident_pairs() {
-  static int n = 0;
-  if (!n) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * 256);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemP;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, ffn_pair_kernel, &cfg) != cudaSuccess || clusters < 1) {
-      cudaGetLastError();
-      clusters = num_sms() / 2;
-    }
-    n = clusters < num_sms() / 2 ? clusters : num_sms() / 2;
-  }
-  return n;
+// Clusters of 2 that can be resident at once on the current device (every
+// pair must be, for the GEMM2 tiles' waits to end). The first call on a device
+// also opts the kernel in to its shared-memory size there.
+cudaError_t resident_pairs(int *out) {
+  static PerDevice<int> cache;
+  return cache.get(
+      [](int *n) {
+        cudaError_t e = cudaFuncSetAttribute(ffn_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemP);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * 256);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmemP;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, ffn_pair_kernel, &cfg) != cudaSuccess || clusters < 1) {
+          cudaGetLastError();
+          clusters = num_sms() / 2;
+        }
+        *n = clusters < num_sms() / 2 ? clusters : num_sms() / 2;
+        return cudaSuccess;
+      },
+      out);
 }
 
 }  // namespace
@@ -635,12 +640,9 @@ cudaError_t launch_ffn_tc(const Dims &D, const void *x_perm, int64_t a_rows, con
                           void *y_perm, int32_t *blk_done, int32_t *status, cudaStream_t s) {
   if (D.dt != MOE_DT_BF16 || D.N > kMaxExperts || D.d > (1 << 30) || D.d_ff > (1 << 30) || !blk_done)
     return cudaErrorNotSupported;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(ffn_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemP);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  int pairs = 0;
+  const cudaError_t pe = resident_pairs(&pairs);  // also sets the kernel's shared-memory size on this device
+  if (pe != cudaSuccess) return pe;
   CUtensorMap tx, tw1, th, tw2, ths;
   const uint64_t dx[2] = {(uint64_t)D.d, (uint64_t)a_rows};  // rows past a_rows read as zeros
   const uint64_t dw1[3] = {(uint64_t)D.d, (uint64_t)D.d_ff, (uint64_t)D.N};
@@ -650,7 +652,6 @@ cudaError_t launch_ffn_tc(const Dims &D, const void *x_perm, int64_t a_rows, con
       !make_map(&tw2, w2, 3, dw2, 128) || !make_map(&ths, h, 2, dh, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   const int64_t max_pairs = (int64_t)ffn_blocks_max(D) * (((D.d_ff + BNP - 1) / BNP) + ((D.d + BNP - 1) / BNP));
-  int pairs = resident_pairs();
   if (max_pairs < pairs) pairs = (int)max_pairs;
   if (pairs < 1) pairs = 1;
   return launch_k(ffn_pair_kernel, dim3(2 * pairs), dim3(kThreads), kSmemP, s, 2u, tx, tw1, th, tw2, ths, offsets,

@@ -247,6 +247,24 @@ moe_status do_shared(const Dims &D, const moe_workspace_layout &L, const void *x
 
 void moe::set_last_error(const char *text) { snprintf(g_err, sizeof(g_err), "%s", text); }
 
+int moe::num_sms() {
+  static PerDevice<int> cache;
+  int n = 0;
+  const cudaError_t e = cache.get(
+      [](int *v) {
+        int dev = 0;
+        cudaError_t r = cudaGetDevice(&dev);
+        if (r == cudaSuccess) r = cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, dev);
+        if (r != cudaSuccess || *v <= 0) {
+          cudaGetLastError();
+          *v = 148;
+        }
+        return cudaSuccess;
+      },
+      &n);
+  return e == cudaSuccess && n > 0 ? n : 148;
+}
+
 extern "C" {
 
 const char *moe_version(void) { return "sparse-moe-b300 0.1 (sm_103a)"; }
@@ -451,6 +469,18 @@ moe_status moe_forward_shared(const moe_config *cfg, const void *x, const void *
   TRY(do_ffn(D, L, x_perm, offsets, w1, b1, w2, b2, row_gate, AT(ws, L.h, void *), y_perm, ws, s));
   TRY(do_shared(D, L, x, sw1, sb1, sw2, sb2, ws, s));
   TRY(do_combine(D, L, y_perm, row_of, gate, x, y, ws, s));
+  return MOE_OK;
+}
+
+moe_status moe_selftest_wait_timeout(void *ws, int64_t limit_ns, int32_t *result, moe_stream_t stream) {
+  TRY(check_ptrs({ws, result}, "moe_selftest_wait_timeout"));
+  if (limit_ns < 1000 || limit_ns > 1000000000)
+    return fail(MOE_ERR_INVALID_ARG, "limit_ns must be in [1000, 1e9] (got %lld)", (long long)limit_ns);
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemsetAsync(result, 0, 8 * sizeof(int32_t), s);
+  if (e == cudaSuccess)
+    e = launch_wait_expiry(static_cast<int32_t *>(ws), result + 4, (unsigned long long)limit_ns, result, s);
+  if (e != cudaSuccess) return cuda_fail(e, "wait self-test");
   return MOE_OK;
 }
 

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <utility>
 
 #include "moe.h"
@@ -29,7 +30,47 @@ enum KernelId : int32_t {
   kKCombine = 6,
   kKGemmTc = 7,
   kKGemmTcDecode = 8,
+  kKSelfTest = 9,
 };
+
+// ---- per-device host state ---------------------------------------------
+// One-time facts and settings that belong to a device (its SM count, a
+// kernel's opt-in shared-memory size, how many clusters fit at once) are kept
+// per device: one process may drive several GPUs, and cudaFuncSetAttribute
+// applies only to the device that is current when it is called. A value is
+// made once per device, with that device current, under a lock, so first
+// calls from several host threads are safe.
+constexpr int kMaxDevices = 64;
+
+template <typename T> class PerDevice {
+ public:
+  // *out = the current device's value; make(T *) fills it on first use and
+  // returns a cudaError_t (the value is kept only when make succeeds).
+  template <typename Make> cudaError_t get(Make &&make, T *out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (!ready_[dev]) {
+      T v{};
+      e = make(&v);
+      if (e != cudaSuccess) return e;
+      val_[dev] = v;
+      ready_[dev] = true;
+    }
+    *out = val_[dev];
+    return cudaSuccess;
+  }
+
+ private:
+  std::mutex mu_;
+  bool ready_[kMaxDevices] = {};
+  T val_[kMaxDevices] = {};
+};
+
+// Streaming multiprocessors of the current device (148 if it cannot be read).
+int num_sms();
 
 struct Dims {
   int64_t T, d, d_ff;
@@ -235,6 +276,11 @@ inline int64_t ffn_sync_ints(const Dims &D) {
 cudaError_t launch_ffn_tc(const Dims &D, const void *x_perm, int64_t a_rows, const int32_t *offsets, const void *w1,
                           const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
                           void *y_perm, int32_t *blk_done, int32_t *status, cudaStream_t s);
+
+// Self-test of the bounded waits: one CTA waits on an mbarrier nothing arms
+// and on a counter (*counter stays 0) nothing raises, each for limit_ns.
+cudaError_t launch_wait_expiry(int32_t *status, const int32_t *counter, unsigned long long limit_ns,
+                               int32_t *result, cudaStream_t s);
 
 // Expert-choice requests: idx[t * N + j] = j for every token.
 cudaError_t launch_ec_pattern(int32_t *idx, int64_t T, int N, cudaStream_t s);

@@ -349,14 +349,16 @@ __global__ void __launch_bounds__(kRThreads, 1)
 template <int NP, int S>
 cudaError_t launch_np(const Dims &D, const void *x, const void *w_g, const float *router_bias, int32_t *topk_idx,
                       float *gate, float *score, float *probs, float *lse, int32_t *status, cudaStream_t s) {
-  static bool attr_set = false;
+  static PerDevice<int> attr;  // this instance's shared-memory size, set once per device
   const size_t smem = router_smem<NP, S>();
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(router_tc_kernel<NP, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  int set = 0;
+  const cudaError_t ae = attr.get(
+      [smem](int *v) {
+        *v = 1;
+        return cudaFuncSetAttribute(router_tc_kernel<NP, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      },
+      &set);
+  if (ae != cudaSuccess) return ae;
   CUtensorMap tx, tw;
   const uint64_t dx[2] = {(uint64_t)D.d, (uint64_t)D.T};
   const uint64_t dw[2] = {(uint64_t)D.d, (uint64_t)D.N};

@@ -43,17 +43,18 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long *bar, uint32_t 
 }
 
 // Bounded wait for the phase of the given parity. Returns false (and raises
-// the CTA's abort flag, recording MOE_ERR_TIMEOUT once) when the limit passes,
+// the CTA's abort flag, recording MOE_ERR_TIMEOUT once) when limit_ns passes,
 // or when another role has aborted.
 static __device__ __noinline__ bool mbar_wait(unsigned long long *bar, uint32_t parity, volatile int *abort,
-                                       int32_t *status, int kernel, int where) {
+                                       int32_t *status, int kernel, int where,
+                                       unsigned long long limit_ns = kTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
       if (*abort) return false;
-      if (globaltimer() - t0 > kTimeoutNs) {
+      if (globaltimer() - t0 > limit_ns) {
         report_error(status, MOE_ERR_TIMEOUT, kernel, where);
         *abort = 1;
         return false;
@@ -77,15 +78,15 @@ __device__ __forceinline__ int ld_acquire(const int32_t *p) {
   asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-// Bounded wait until *p >= need (acquire). False on timeout (MOE_ERR_TIMEOUT
-// recorded, abort raised) or when another role has aborted.
+// Bounded wait until *p >= need (acquire). False on timeout after limit_ns
+// (MOE_ERR_TIMEOUT recorded, abort raised) or when another role has aborted.
 static __device__ __noinline__ bool wait_counter(const int32_t *p, int need, volatile int *abort, int32_t *status,
-                                          int kernel, int where) {
+                                          int kernel, int where, unsigned long long limit_ns = kTimeoutNs) {
   if (ld_acquire(p) >= need) return true;
   const unsigned long long t0 = globaltimer();
   while (ld_acquire(p) < need) {
     if (*abort) return false;
-    if (globaltimer() - t0 > kTimeoutNs) {
+    if (globaltimer() - t0 > limit_ns) {
       report_error(status, MOE_ERR_TIMEOUT, kernel, where);
       *abort = 1;
       return false;
@@ -183,16 +184,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 
 // ---- host side --------------------------------------------------------------
+// The driver's tensor-map encoder (process-wide: it does not depend on the
+// device); looked up once, thread-safely.
 inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
     void *p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
-  }
+      return (PFN_cuTensorMapEncodeTiled_v12000)p;
+    return nullptr;
+  }();
   return fn;
 }
 
@@ -211,17 +214,6 @@ inline bool make_map(CUtensorMap *m, const void *ptr, int rank, const uint64_t *
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(ptr), gd, gs, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-inline int num_sms() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
 }
 
 }  // namespace tc

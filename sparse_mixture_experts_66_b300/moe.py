@@ -67,7 +67,7 @@ class MoeWorkspaceLayout(ctypes.Structure):
 
 
 # Names and argument kinds of every symbol the header declares.
-# kinds: C = config*, P = device pointer, S = stream, L = layout*.
+# kinds: C = config*, P = device pointer, S = stream, L = layout*, I = int64.
 SIGNATURES = {
     "moe_version": ([], ctypes.c_char_p),
     "moe_last_error": ([], ctypes.c_char_p),
@@ -85,9 +85,10 @@ SIGNATURES = {
     "moe_router_stats": (["C"] + ["P"] * 5 + ["S"], ctypes.c_int),
     "moe_shared_expert": (["C"] + ["P"] * 6 + ["S"], ctypes.c_int),
     "moe_forward_shared": (["C"] + ["P"] * 13 + ["S"], ctypes.c_int),
+    "moe_selftest_wait_timeout": (["P", "I", "P", "S"], ctypes.c_int),
 }
 _KIND = {"C": ctypes.POINTER(MoeConfig), "P": ctypes.c_void_p, "S": ctypes.c_void_p,
-         "L": ctypes.POINTER(MoeWorkspaceLayout)}
+         "L": ctypes.POINTER(MoeWorkspaceLayout), "I": ctypes.c_int64}
 
 _lib = None
 
@@ -227,6 +228,12 @@ def moe_forward_noalloc(cfg, x, w_g, router_bias, w1, b1, w2, b2, y, stream=None
     on the shared array."""
     _check(load().moe_forward_noalloc(ctypes.byref(cfg), _ptr(x), _ptr(w_g), _ptr(router_bias), _ptr(w1), _ptr(b1),
                                       _ptr(w2), _ptr(b2), _ptr(y), _stream(stream)))
+
+
+def moe_selftest_wait_timeout(ws, limit_ns, result, stream=None):
+    """Run the bounded-wait self-test: both waits must give up after limit_ns
+    and leave MOE_ERR_TIMEOUT in ws's status word; result is a device int32[8]."""
+    _check(load().moe_selftest_wait_timeout(_ptr(ws), ctypes.c_int64(int(limit_ns)), _ptr(result), _stream(stream)))
 
 
 # ---- workspace helper -------------------------------------------------------

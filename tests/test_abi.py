@@ -180,3 +180,15 @@ def test_expert_choice_flag_rules():
     assert L.row_token - L.row_of >= 64 * 8 * 4
     C = moe.moe_capacity(cfg)
     assert C == 20 and L.rows >= 8 * 128  # C = ceil(1.25 * 64 * 2 / 8)
+
+
+def test_selftest_checks_its_limit_before_touching_the_device():
+    """The wait self-test validates its arguments on the host: a limit outside
+    [1 us, 1 s] returns MOE_ERR_INVALID_ARG before anything is enqueued (so
+    this runs without a GPU, on placeholder aligned pointers)."""
+    lib = moe.load()
+    for bad in (0, 999, 1_000_000_001):
+        st = lib.moe_selftest_wait_timeout(ctypes.c_void_p(256), ctypes.c_int64(bad), ctypes.c_void_p(512), None)
+        assert st == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_selftest_wait_timeout(None, ctypes.c_int64(10_000), ctypes.c_void_p(512), None) == \
+        moe.MOE_ERR_INVALID_ARG

@@ -48,3 +48,36 @@ def test_reference_arm_prints_one_json_line():
     assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "tokens/s"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+    # the timing it reports is the time it spent: the whole small batch ran each step
+    assert not d["extrapolated"] and d["tokens_per_timed_step"] == 256
+    assert abs(d["timed_region_s"] - d["ms_per_step"] * 1e-3 * d["steps"]) < 1e-9
+
+
+def test_gpus_flag_launches_one_rank_per_gpu():
+    """bench.py --gpus 2 without a launcher re-runs itself under
+    torch.distributed.run with two ranks; on the host-core arm rank 0 alone
+    prints the line, which reports both ranks, and the other rank exits 0."""
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--impl", "reference", "--steps", "1",
+           "--warmup", "1", "--workload", "f32_T256_d64_N4_k1_dff256_cf1.25", "--ref-budget", "2"]
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    p = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT, env=env)
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [l for l in p.stdout.strip().splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1, p.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2
+    assert d["config"]["parallelism"] == "replicas2"
+
+
+def test_both_arms_report_the_same_config():
+    """The reference arm's config is built by the same function as the GPU
+    arm's, from the oracle's capacity and kept counts."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from sparse_mixture_experts_66_b300.workload import WORKLOADS
+
+    w = WORKLOADS["f32_T256_d64_N4_k1_dff256_cf1.25"]
+    cfg = bench.config_dict(w, 80, [64, 64, 64, 64], 1)
+    assert cfg["kept_rows"] == 256 and cfg["active_experts"] == 4 and cfg["capacity"] == 80
+    assert set(cfg) == {"workload", "T", "d", "N", "k", "d_ff", "capacity_factor", "router_bias", "capacity",
+                        "kept_rows", "active_experts", "parallelism", "l2"}

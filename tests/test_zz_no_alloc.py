@@ -9,7 +9,6 @@ process: the first call sets the scratch address up on the device.
 """
 import math
 
-import numpy as np
 import pytest
 import torch
 
@@ -18,7 +17,6 @@ from sparse_mixture_experts_66_b300.workload import SMALL_FP32, WORKLOADS, custo
 
 pytestmark = pytest.mark.gpu
 
-TOL = {"f32": 1e-4, "bf16": 2e-2}  # the parity tolerance of the other GPU tests
 CASES = [WORKLOADS[SMALL_FP32], custom(300, 256, 512, 8, 2, 1.0, router_bias="zipf", seed=21)]
 
 
@@ -50,10 +48,11 @@ def test_noalloc_matches_moe_forward_on_two_calls_in_a_row(w):
     torch.cuda.synchronize()
     for x, y in zip(batches, outs):
         ref = _reference(cfg, d, x)
-        a, b = y.float().cpu().numpy(), ref.float().cpu().numpy()
-        assert np.all(np.isfinite(a))
-        scale = float(np.max(np.abs(b)))
-        assert float(np.max(np.abs(a - b))) <= TOL[w.dtype] * scale
+        assert torch.all(torch.isfinite(y))
+        # the same launches on the same inputs, and no atomics decide any
+        # output: anything but bit equality is a bug (e.g. stale scratch
+        # carried over from the previous call)
+        assert torch.equal(y, ref)
 
 
 def test_noalloc_rejects_configs_beyond_its_scratch():
