@@ -114,6 +114,20 @@ __device__ __forceinline__ void stv(__nv_bfloat16 *p, const float (&v)[W]) {
   else *reinterpret_cast<uint2 *>(p) = make_uint2(w[0], w[W / 2 - 1]);
 }
 
+// A 16-byte vector as W values of T, widened exactly to fp32.
+template <typename T, int W> __device__ __forceinline__ void widen(uint4 q, float (&v)[W]);
+template <> __device__ __forceinline__ void widen<float, 4>(uint4 q, float (&v)[4]) {
+  v[0] = __uint_as_float(q.x); v[1] = __uint_as_float(q.y); v[2] = __uint_as_float(q.z); v[3] = __uint_as_float(q.w);
+}
+template <> __device__ __forceinline__ void widen<__nv_bfloat16, 8>(uint4 q, float (&v)[8]) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
 // Combine, without K slices: a CTA owns U = 8 / KM tokens (KM >= k); its
 // threads take W columns at a time (8 for bf16, 4 for fp32). The
 // CTA reads the U x KM row indices once and turns them into source-row
@@ -160,19 +174,16 @@ __global__ void __launch_bounds__(kC8Threads) combine_kernel(const T *__restrict
     renorm[u] = (flags & MOE_FLAG_RENORM_SURVIVORS) && nkept > 0;
     ident[u] = (flags & MOE_FLAG_IDENTITY_FALLBACK) && nkept == 0;
   }
+  static_assert(W * sizeof(T) == 16, "one 16-byte vector per source row and step");
   for (int64_t c = (int64_t)threadIdx.x * W; c < d; c += kC8Threads * W) {
-    float v[U][KM][W];
+    // raw 16-byte vectors (widened only when added: half the registers of
+    // holding them as fp32, so more CTAs stay resident)
+    uint4 raw[U][KM];
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
-      for (int j = 0; j < KM; ++j) {
-        if (src[u][j]) {
-          ldv<W>(src[u][j] + c, v[u][j]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < W; ++i) v[u][j][i] = 0.f;
-        }
-      }
+      for (int j = 0; j < KM; ++j)
+        raw[u][j] = src[u][j] ? __ldg(reinterpret_cast<const uint4 *>(src[u][j] + c)) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       if (!live[u]) continue;
@@ -181,9 +192,12 @@ __global__ void __launch_bounds__(kC8Threads) combine_kernel(const T *__restrict
       for (int i = 0; i < W; ++i) a[i] = 0.f;
 #pragma unroll
       for (int j = 0; j < KM; ++j)
-        if (src[u][j])
+        if (src[u][j]) {
+          float v[W];
+          widen<T, W>(raw[u][j], v);
 #pragma unroll
-          for (int i = 0; i < W; ++i) a[i] += v[u][j][i];
+          for (int i = 0; i < W; ++i) a[i] += v[i];
+        }
       if (renorm[u])
 #pragma unroll
         for (int i = 0; i < W; ++i) a[i] /= ksum[u];
@@ -352,13 +366,12 @@ cudaError_t launch_combine_t(const Dims &D, const T *y_perm, const float *y_spli
   const int km = D.k <= 1 ? 1 : D.k <= 2 ? 2 : D.k <= 4 ? 4 : 8;
   const int64_t tok_per_block = 8 / km;
   const unsigned g = (unsigned)((D.T + tok_per_block - 1) / tok_per_block);
-  // bf16: 8 columns (16-byte loads and stores); fp32: 4 (16-byte loads, and
-  // twice the active threads on narrow rows)
-  const bool w8 = sizeof(T) == 2;
-  auto kern = km == 1   ? (w8 ? combine_kernel<T, 1, 8> : combine_kernel<T, 1, 4>)
-              : km == 2 ? (w8 ? combine_kernel<T, 2, 8> : combine_kernel<T, 2, 4>)
-              : km == 4 ? (w8 ? combine_kernel<T, 4, 8> : combine_kernel<T, 4, 4>)
-                        : (w8 ? combine_kernel<T, 8, 8> : combine_kernel<T, 8, 4>);
+  // one 16-byte vector per thread and source row: 8 bf16 or 4 fp32 columns
+  constexpr int W = 16 / (int)sizeof(T);
+  auto kern = km == 1   ? combine_kernel<T, 1, W>
+              : km == 2 ? combine_kernel<T, 2, W>
+              : km == 4 ? combine_kernel<T, 4, W>
+                        : combine_kernel<T, 8, W>;
   return launch_k(kern, dim3(g), dim3(kC8Threads), 0, s, 1u, y_perm, D.d, row_of, gate, x, y_shared, D.T, D.k,
                   D.R_max, D.flags, y, status);
 }

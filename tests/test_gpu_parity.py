@@ -34,10 +34,16 @@ STAGE_CASES = [
     custom(512, 64, 64, 256, 8, 1.0, seed=4),
     # every fp32 score of expert 0 rounds to 1.0: a full tie, resolved by token order
     custom(400, 128, 256, 8, 2, 1.0, router_bias="const:0:30", seed=9),
-    # more requests than one pass of the capacity CTA holds: compacted per expert, with overflow
+    # more requests than one pass of the capacity CTA holds (8192): two chunks, compacted per expert, with overflow
     custom(6000, 64, 64, 8, 2, 1.0, router_bias="zipf", seed=17),
-    # expert 0 receives more requests than the compacted list holds (16384): the multi-pass fallback
+    # 32000 requests: an expert's shared-memory list holds T = 16000 entries (a token's picks are distinct
+    # experts), and expert 0 receives nearly all tokens
+    custom(16000, 64, 64, 4, 2, 1.0, router_bias="const:0:6", seed=22),
+    # k = 1 with 17000 requests: the list holds every request (close to its largest size for N = 2)
+    custom(17000, 64, 64, 2, 1, 0.75, router_bias="const:1:3", seed=20),
+    # T = 20000 and 24000: more tokens than a list holds, the streaming form of the kernel runs
     custom(20000, 64, 64, 4, 2, 1.0, router_bias="const:0:6", seed=18),
+    custom(24000, 64, 64, 4, 2, 1.0, router_bias="const:0:6", seed=19),
 ]
 
 
@@ -211,10 +217,14 @@ def test_deterministic_across_runs():
     assert np.array_equal(a["row_of"], b["row_of"])
 
 
-def test_stage_calls_compose_to_forward():
+@pytest.mark.parametrize("w", [
+    custom(700, 256, 512, 8, 2, 1.0, router_bias="zipf", seed=15),
+    # decode-shaped: the swap-AB expert FFN and the K-sliced combine
+    custom(64, 1024, 4096, 8, 2, math.inf, seed=23),
+], ids=lambda w: w.name)
+def test_stage_calls_compose_to_forward(w):
     """moe_route + moe_dispatch + moe_expert_ffn + moe_combine on caller
     buffers give the same bits as moe_forward."""
-    w = custom(700, 256, 512, 8, 2, 1.0, router_bias="zipf", seed=15)
     inp = draw(w)
     g = parity.run_gpu(w, inp)
     dev, cfg = g["_dev"], g["_cfg"]
