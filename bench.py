@@ -3,7 +3,8 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
 One step = one full layer forward (router, capacity + dispatch, expert FFNs,
-combine) over one batch of the workload, inputs resident in HBM. The default
+combine) over one batch of the workload, inputs resident in HBM, replayed as a
+CUDA graph of those launches. The default
 workload is the largest single-GPU one: the bf16 prefill shape T=16384,
 d=4096, N=8, k=2, d_ff=14336 with no capacity limit. The step is
 issued as the four stage calls of the C ABI (moe_route, moe_dispatch,
@@ -13,7 +14,8 @@ launching stream; a second timed region of the same K steps puts events around
 the expert FFN launch for its roofline, and a third pass with an event after
 every stage gives the stage breakdown. Between timed steps L2 is flushed (a
 512 MiB write, then a 1 GiB read, outside the events) unless a step streams at
-least twice the L2 size, in which case its inputs are larger than L2. ``e2e`` times
+least twice the L2 size, in which case its inputs are larger than L2. The
+roofline and stage-breakdown regions launch the stage calls directly. ``e2e`` times
 moe_forward with each step's batch copied in from pinned host memory and its
 output copied back inside the timed region, the copies of neighbouring steps
 overlapping the forward on a second stream (double-buffered x and y).
@@ -288,9 +290,23 @@ def run_ours(args, world, rank, local):
     use_flush, _ = l2_policy(w, alg["bytes"])
 
     K = args.steps
-    # Timed region 1 (the value): events at the step boundaries only, so the
-    # launches inside a step overlap through programmatic dependent launch as
-    # they do for a user.
+    # The step as a CUDA graph: the four stage calls (the launches moe_forward
+    # makes) captured once and replayed once per step, as a serving loop
+    # would; the programmatic-dependent-launch edges between the kernels are
+    # kept in the graph.
+    graph = torch.cuda.CUDAGraph()
+    cap_stream = torch.cuda.Stream(device)
+    cap_stream.wait_stream(stream)
+    with torch.cuda.graph(graph, stream=cap_stream):
+        st.all(cap_stream)
+    stream.wait_stream(cap_stream)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize(device)
+    ws.status(stream)
+    # Timed region 1 (the value): events at the step boundaries only, around
+    # each replay, so the launches inside a step overlap through programmatic
+    # dependent launch as they do for a user.
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     clocks = ClockSampler(local)
     clocks.start()
@@ -302,7 +318,7 @@ def run_ours(args, world, rank, local):
             flush()  # evict L2 between steps, outside the step's events
         e = ev[i]
         e[0].record(stream)
-        st.all(stream)
+        graph.replay()
         e[1].record(stream)
     torch.cuda.synchronize(device)
     barrier(world)
@@ -455,7 +471,8 @@ def run_ours(args, world, rank, local):
                  "frac_tensor_roofline": (alg["flops"] / (peaks["bf16_tflops"] * 1e12)) / (ms * 1e-3),
                  "frac_hbm_roofline": (alg["bytes"] / (peaks["hbm_gbs"] * 1e9)) / (ms * 1e-3),
                  "stages_ms": stage_ms, "ms_min": min(step_ms), "ms_median": statistics.median(step_ms),
-                 "wall_s": t_wall},
+                 "wall_s": t_wall,
+                 "timing": "CUDA events around each replay of a CUDA graph of one forward's launches"},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": w.T * w.d * es,
                 "d2h_bytes_per_step": w.T * w.d * es, "ms_per_step": e2e_ms, "mode": e2e_mode},
         "gpu_launches": kernels_per_step(w) * K,

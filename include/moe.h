@@ -113,8 +113,9 @@ typedef struct {
 
 /* Byte offsets of the buffers inside a workspace (all 256-byte aligned).
  * rows = R_max, the row capacity of the permuted buffers: every expert segment
- * starts on a multiple of 128 rows (64 rows for decode-shaped configs: bf16
- * with T*k <= 64*N), so R_max = floor((min(T*k, N*C) + 127*N) / 128) * 128
+ * starts on a multiple of 128 rows (for decode-shaped configs, bf16 with
+ * T*k <= 64*N: 64 rows, or 32 rows when T*k <= 16*N), so
+ * R_max = floor((min(T*k, N*C) + 127*N) / 128) * 128
  * bounds the rows in use. */
 typedef struct {
   size_t status;      /* int32[16]; [0] first device error code, [1] kernel id, [2] detail */
@@ -202,7 +203,8 @@ moe_status moe_router_stats(const moe_config *cfg, void *ws, const int32_t *coun
 /* Steps 4-5: capacity enforcement and dispatch. Per expert, keep the top C
  * requests by (score desc, token asc); number the kept rows of each expert in
  * ascending token order inside a segment that starts at offsets[e] (a
- * multiple of 128 rows); gather x into those rows (padding rows are zero).
+ * multiple of 128 rows, or of the decode chunk size for decode-shaped configs:
+ * see moe_workspace_layout); gather x into those rows (padding rows are zero).
  *   in:  x [T, d], topk_idx, gate, score [T, k] (as written by moe_route);
  *   out: counts_raw [N], counts_kept [N], offsets [N+1], row_of [T, k],
  *        row_token [rows], row_gate [rows] (the gate of each kept pick; 0

@@ -39,21 +39,17 @@ namespace {
 using namespace tc;
 
 constexpr int kDM = 128;  // weight rows per tile (MMA M)
-constexpr int kDN = 64;   // token rows per chunk (MMA N)
 constexpr int kDAtom = 64;                // columns of one 128-byte swizzle atom (one TMA box)
 constexpr int kDAtoms = 2;                // atoms per stage: each weight row is requested 256 B at a time
 constexpr int kDBK = kDAtom * kDAtoms;    // k-block
-constexpr int kDStages = 8 / kDAtoms;
 constexpr int kDWAtomBytes = kDM * kDAtom * 2;
-constexpr int kDTAtomBytes = kDN * kDAtom * 2;
 constexpr int kDWBytes = kDWAtomBytes * kDAtoms;
-constexpr int kDTBytes = kDTAtomBytes * kDAtoms;
-constexpr int kDStageBytes = kDWBytes + kDTBytes;
 constexpr int kDThreads = 192;
 constexpr int kDMaxExperts = 256;
+constexpr int kDMaxStages = 5;
 
 struct DCtrl {
-  unsigned long long full[kDStages], empty[kDStages], tfull[2], tempty[2], drain;
+  unsigned long long full[kDMaxStages], empty[kDMaxStages], tfull[2], tempty[2], drain;
   uint32_t tmem_base;
   int abort;
   int total1, total2;  // GEMM1 tiles, GEMM1 + GEMM2 tiles
@@ -67,9 +63,20 @@ struct DTile {
   int e, row0, m, sp;
 };
 
-constexpr size_t kDSmem = 1024 + (size_t)kDStages * kDStageBytes + sizeof(DCtrl);
+// Token chunks of DN rows (MMA N): 64, or 32 when experts hold few rows, which
+// leaves room for a fifth stage (more weight bytes in flight per SM).
+template <int DN> struct DCfg {
+  static constexpr int kStages = DN == 32 ? 5 : 4;
+  static constexpr int kTAtomBytes = DN * kDAtom * 2;
+  static constexpr int kTBytes = kTAtomBytes * kDAtoms;
+  static constexpr int kStageBytes = kDWBytes + kTBytes;
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + sizeof(DCtrl);
+  static_assert(kStages <= kDMaxStages, "barrier arrays");
+  static_assert(kSmem <= 227 * 1024, "shared memory");
+};
 
 // Tiles of expert e: chunks_e x slices x m_tiles, m fastest, then the slice.
+template <int DN>
 __device__ __forceinline__ DTile decode_tile(const DCtrl *c, int N_exp, int m1, int m2, int S, int t) {
   DTile d;
   d.phase = t >= c->total1 ? 1 : 0;
@@ -86,10 +93,11 @@ __device__ __forceinline__ DTile decode_tile(const DCtrl *c, int N_exp, int m1, 
   d.m = local % mt;
   local /= mt;
   d.sp = local % sl;
-  d.row0 = c->offsets[lo] + (local / sl) * kDN;
+  d.row0 = c->offsets[lo] + (local / sl) * DN;
   return d;
 }
 
+template <int DN>
 __global__ void __launch_bounds__(kDThreads, 1)
     ffn_decode_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_x,
                       const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_h,
@@ -98,11 +106,12 @@ __global__ void __launch_bounds__(kDThreads, 1)
                       const float *__restrict__ row_gate, __nv_bfloat16 *__restrict__ h,
                       __nv_bfloat16 *__restrict__ y_perm,
                       float *__restrict__ y_split, int32_t *__restrict__ h_done, int32_t *status) {
+  using C = DCfg<DN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t *sW = base;
-  uint8_t *sT = base + kDStages * kDWBytes;
-  DCtrl *c = (DCtrl *)(base + kDStages * kDStageBytes);
+  uint8_t *sT = base + C::kStages * kDWBytes;
+  DCtrl *c = (DCtrl *)(base + C::kStages * C::kStageBytes);
   volatile int *abort = &c->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m1 = (d_ff + kDM - 1) / kDM, m2 = (d + kDM - 1) / kDM;
@@ -119,10 +128,10 @@ __global__ void __launch_bounds__(kDThreads, 1)
       n1[i] = n2[i] = 0;
       if (e < N_exp) {
         const int o0 = offsets_g[e], o1 = offsets_g[e + 1];
-        if (o1 < o0 || (o1 - o0) % kDN != 0 || o1 > R_max) bad = true;
+        if (o1 < o0 || (o1 - o0) % DN != 0 || o1 > R_max) bad = true;
         else {
-          n1[i] = (o1 - o0) / kDN * m1;
-          n2[i] = (o1 - o0) / kDN * S * m2;
+          n1[i] = (o1 - o0) / DN * m1;
+          n2[i] = (o1 - o0) / DN * S * m2;
         }
       }
       s1 += n1[i];
@@ -163,7 +172,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      for (int s = 0; s < kDStages; ++s) {
+      for (int s = 0; s < C::kStages; ++s) {
         mbar_init(&c->full[s], 1);
         mbar_init(&c->empty[s], 1);
       }
@@ -176,7 +185,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
     }
     __syncwarp();
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&c->tmem_base)),
-                 "r"(2 * kDN));
+                 "r"(2 * DN));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   tc_fence_before();
@@ -193,13 +202,13 @@ __global__ void __launch_bounds__(kDThreads, 1)
       uint32_t issued_mask = 0, parity_mask = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-        const DTile tl = decode_tile(c, N_exp, m1, m2, S, t);
+        const DTile tl = decode_tile<DN>(c, N_exp, m1, m2, S, t);
         int kb0 = 0, kb1 = kb1_count;
         if (tl.phase) {
           kb0 = tl.sp * kb2_count / S;
           kb1 = (tl.sp + 1) * kb2_count / S;
           // every GEMM1 tile of this expert must have stored its rows of h
-          const int need = (c->offsets[tl.e + 1] - c->offsets[tl.e]) / kDN * m1 * 4;
+          const int need = (c->offsets[tl.e + 1] - c->offsets[tl.e]) / DN * m1 * 4;
           if (!wait_counter(h_done + tl.e, need, abort, status, kKGemmTcDecode, 5)) {
             ok = false;
             break;
@@ -211,7 +220,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
             ok = false;
             break;
           }
-          mbar_expect_tx(&c->full[s], kDStageBytes);
+          mbar_expect_tx(&c->full[s], C::kStageBytes);
           const CUtensorMap *mw = tl.phase ? &tm_w2 : &tm_w1;
           const CUtensorMap *mt = tl.phase ? &tm_h : &tm_x;
 #pragma unroll
@@ -220,17 +229,17 @@ __global__ void __launch_bounds__(kDThreads, 1)
                         tl.e);
 #pragma unroll
           for (int a = 0; a < kDAtoms; ++a)
-            tma_load_2d(sT + s * kDTBytes + a * kDTAtomBytes, mt, &c->full[s], kb * kDBK + a * kDAtom, tl.row0);
+            tma_load_2d(sT + s * C::kTBytes + a * C::kTAtomBytes, mt, &c->full[s], kb * kDBK + a * kDAtom, tl.row0);
           issued_mask |= 1u << s;
           parity_mask = (parity_mask & ~(1u << s)) | (ph << s);
-          if (++s == kDStages) {
+          if (++s == C::kStages) {
             s = 0;
             ph ^= 1u;
           }
         }
       }
       if (!ok) {
-        for (int i = 0; i < kDStages; ++i)
+        for (int i = 0; i < C::kStages; ++i)
           if (issued_mask & (1u << i)) {
             const unsigned long long ts = globaltimer();
             while (!mbar_try_wait(&c->full[i], (parity_mask >> i) & 1u) && globaltimer() - ts < kTimeoutNs) {
@@ -244,11 +253,11 @@ __global__ void __launch_bounds__(kDThreads, 1)
       uint32_t ph = 0, aph = 0;
       int acc = 0;
       bool ok = true, any = false;
-      const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kDN >> 3) << 17) |
+      const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(DN >> 3) << 17) |
                              ((uint32_t)(kDM >> 4) << 24);
       const uint64_t wdesc0 = smem_desc_sw128(saddr(sW)), tdesc0 = smem_desc_sw128(saddr(sT));
       for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-        const DTile tl = decode_tile(c, N_exp, m1, m2, S, t);
+        const DTile tl = decode_tile<DN>(c, N_exp, m1, m2, S, t);
         int kb0 = 0, kb1 = kb1_count;
         if (tl.phase) {
           kb0 = tl.sp * kb2_count / S;
@@ -256,7 +265,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
         }
         if (!mbar_wait_fast(&c->tempty[acc], aph ^ 1u, abort, status, kKGemmTcDecode, 20 + acc)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + (uint32_t)(acc * kDN);
+        const uint32_t d_tmem = tmem + (uint32_t)(acc * DN);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_fast(&c->full[s], ph, abort, status, kKGemmTcDecode, 30 + s)) {
             ok = false;
@@ -267,12 +276,12 @@ __global__ void __launch_bounds__(kDThreads, 1)
           for (int kk = 0; kk < kDBK / 16; ++kk)
             umma_bf16_cta1(d_tmem,
                            wdesc0 + (uint64_t)(s * (kDWBytes >> 4) + (kk >> 2) * (kDWAtomBytes >> 4) + 2 * (kk & 3)),
-                           tdesc0 + (uint64_t)(s * (kDTBytes >> 4) + (kk >> 2) * (kDTAtomBytes >> 4) + 2 * (kk & 3)),
+                           tdesc0 + (uint64_t)(s * (C::kTBytes >> 4) + (kk >> 2) * (C::kTAtomBytes >> 4) + 2 * (kk & 3)),
                            idesc,
                            (kb != kb0 || kk != 0) ? 1u : 0u);
           any = true;
           umma_commit_cta1(&c->empty[s]);
-          if (++s == kDStages) {
+          if (++s == C::kStages) {
             s = 0;
             ph ^= 1u;
           }
@@ -294,7 +303,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
     int acc = 0;
     uint32_t aph = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const DTile tl = decode_tile(c, N_exp, m1, m2, S, t);
+      const DTile tl = decode_tile<DN>(c, N_exp, m1, m2, S, t);
       // the bias and the chunk's row gates are fetched before the accumulator
       // wait, so no load latency sits between TMEM and the stores
       const int M_out = tl.phase ? d : d_ff;
@@ -306,7 +315,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
       float gate_lo = 1.0f, gate_hi = 1.0f;  // row gates of chunk rows lane and 32 + lane
       if (tl.phase && row_gate) {
         gate_lo = row_gate[tl.row0 + lane];
-        gate_hi = row_gate[tl.row0 + 32 + lane];
+        if (DN > 32) gate_hi = row_gate[tl.row0 + 32 + lane];
       }
       // K slice 0 goes to y_perm (bf16), slices 1..S-1 to y_split (fp32)
       float *dst = tl.phase && tl.sp > 0 ? y_split + (int64_t)(tl.sp - 1) * R_max * d : nullptr;
@@ -316,10 +325,10 @@ __global__ void __launch_bounds__(kDThreads, 1)
       if (!ok) break;
       tc_fence_after();
 #pragma unroll 1
-      for (int c0 = 0; c0 < kDN; c0 += 32) {
+      for (int c0 = 0; c0 < DN; c0 += 32) {
         uint32_t r[32];
         __syncwarp();
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kDN + c0), r);
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * DN + c0), r);
         if (tl.phase == 0) {
           if (fvalid) {
 #pragma unroll
@@ -363,7 +372,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * kDN));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * DN));
   }
   // The last CTA out resets the expert counters (and the exit count) for the
   // next launch: every other CTA has finished all its counter accesses.
@@ -412,12 +421,16 @@ static int64_t max_cta_kblocks(int64_t chunks, int64_t m1, int64_t kb1, int64_t 
   return all + mx;
 }
 
+int decode_chunk_rows(const Dims &D) {
+  return D.T * (int64_t)D.k <= (int64_t)kDecodeSmallRowsPerExpert * D.N ? 32 : 64;
+}
+
 int decode_splits(const Dims &D) {
   if (D.dt != MOE_DT_BF16 || D.T * (int64_t)D.k > (int64_t)kDecodeRowsPerExpert * D.N) return 0;
   // K slices of the second GEMM. The busiest CTA's weight stream sets the
   // time; every slice past the first adds a [rows, d] fp32 partial written
   // here and read by the combine. Pick the S (1..8, at least 4 k-blocks per
-  // slice) that minimises the sum, for one 64-row chunk per routed expert.
+  // slice) that minimises the sum, for one token chunk per routed expert.
   const int64_t m1 = (D.d_ff + kDM - 1) / kDM, m2 = (D.d + kDM - 1) / kDM;
   const int64_t kb1 = (D.d + kDBK - 1) / kDBK, kb2 = (D.d_ff + kDBK - 1) / kDBK;
   const int64_t sms = num_sms();
@@ -428,7 +441,7 @@ int decode_splits(const Dims &D) {
   double best_cost = 0.0;
   for (int64_t S = 1; S <= 8 && (S == 1 || S <= kb2 / 4); ++S) {
     const double cost = (double)max_cta_kblocks(chunks, m1, kb1, m2, kb2, S, sms) * tile_bytes * (double)sms +
-                        (double)(S - 1) * 2.0 * (double)chunks * kDN * (double)D.d * 4.0;
+                        (double)(S - 1) * 2.0 * (double)chunks * decode_chunk_rows(D) * (double)D.d * 4.0;
     if (S == 1 || cost < best_cost) {
       best_cost = cost;
       best = (int)S;
@@ -437,17 +450,19 @@ int decode_splits(const Dims &D) {
   return best;
 }
 
-cudaError_t launch_ffn_decode(const Dims &D, const void *x_perm, const int32_t *offsets, const void *w1,
-                              const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
-                              void *y_perm, float *y_split, int32_t *h_done, int32_t *status, cudaStream_t s) {
-  const int S = decode_splits(D);
-  if (S < 1 || (S > 1 && !y_split) || !h_done || D.N > kDMaxExperts) return cudaErrorNotSupported;
-  static PerDevice<int> attr;  // the kernel's shared-memory size, set once per device
+namespace {
+template <int DN>
+cudaError_t launch_decode_t(const Dims &D, int S, const void *x_perm, const int32_t *offsets, const void *w1,
+                            const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
+                            void *y_perm, float *y_split, int32_t *h_done, int32_t *status, cudaStream_t s) {
+  using C = DCfg<DN>;
+  static PerDevice<int> attr;  // the instance's shared-memory size, set once per device
   int set = 0;
   const cudaError_t ae = attr.get(
       [](int *v) {
         *v = 1;
-        return cudaFuncSetAttribute(ffn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDSmem);
+        return cudaFuncSetAttribute(ffn_decode_kernel<DN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)C::kSmem);
       },
       &set);
   if (ae != cudaSuccess) return ae;
@@ -456,20 +471,33 @@ cudaError_t launch_ffn_decode(const Dims &D, const void *x_perm, const int32_t *
   const uint64_t dx[2] = {(uint64_t)D.d, (uint64_t)D.R_max};
   const uint64_t dw2[3] = {(uint64_t)D.d_ff, (uint64_t)D.d, (uint64_t)D.N};
   const uint64_t dh[2] = {(uint64_t)D.d_ff, (uint64_t)D.R_max};
-  if (!make_map(&tw1, w1, 3, dw1, kDM) || !make_map(&tx, x_perm, 2, dx, kDN) || !make_map(&tw2, w2, 3, dw2, kDM) ||
-      !make_map(&th, h, 2, dh, kDN))
+  if (!make_map(&tw1, w1, 3, dw1, kDM) || !make_map(&tx, x_perm, 2, dx, DN) || !make_map(&tw2, w2, 3, dw2, kDM) ||
+      !make_map(&th, h, 2, dh, DN))
     return cudaErrorInvalidValue;
-  const int64_t chunks = D.R_max / kDN;
+  const int64_t chunks = D.R_max / DN;
   const int64_t max_tiles = chunks * ((D.d_ff + kDM - 1) / kDM) + chunks * S * ((D.d + kDM - 1) / kDM);
   int grid = num_sms();
   if (max_tiles < grid) grid = (int)max_tiles;
   if (grid < 1) grid = 1;
   // One CTA per SM at most (shared memory) and no more CTAs than SMs, so all
   // are resident together: a GEMM2 tile never waits on a CTA that cannot run.
-  return launch_k(ffn_decode_kernel, dim3((unsigned)grid), dim3(kDThreads), kDSmem, s, 1u, tw1, tx, tw2, th, offsets,
-                  (int)D.N, (int64_t)D.R_max, (int)D.d, (int)D.d_ff, S, (const __nv_bfloat16 *)b1,
+  return launch_k(ffn_decode_kernel<DN>, dim3((unsigned)grid), dim3(kDThreads), C::kSmem, s, 1u, tw1, tx, tw2, th,
+                  offsets, (int)D.N, (int64_t)D.R_max, (int)D.d, (int)D.d_ff, S, (const __nv_bfloat16 *)b1,
                   (const __nv_bfloat16 *)b2, row_gate, (__nv_bfloat16 *)h, (__nv_bfloat16 *)y_perm, y_split, h_done,
                   status);
+}
+}  // namespace
+
+cudaError_t launch_ffn_decode(const Dims &D, const void *x_perm, const int32_t *offsets, const void *w1,
+                              const void *b1, const void *w2, const void *b2, const float *row_gate, void *h,
+                              void *y_perm, float *y_split, int32_t *h_done, int32_t *status, cudaStream_t s) {
+  const int S = decode_splits(D);
+  if (S < 1 || (S > 1 && !y_split) || !h_done || D.N > kDMaxExperts) return cudaErrorNotSupported;
+  return decode_chunk_rows(D) == 32
+             ? launch_decode_t<32>(D, S, x_perm, offsets, w1, b1, w2, b2, row_gate, h, y_perm, y_split, h_done,
+                                   status, s)
+             : launch_decode_t<64>(D, S, x_perm, offsets, w1, b1, w2, b2, row_gate, h, y_perm, y_split, h_done,
+                                   status, s);
 }
 
 }  // namespace moe

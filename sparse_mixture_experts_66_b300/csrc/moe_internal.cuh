@@ -16,9 +16,11 @@ namespace moe {
 // many rows, so that a 128-row GEMM tile never spans two experts.
 constexpr int kRowAlign = 128;
 // Decode-shaped batches (at most this many expected rows per expert,
-// T*k <= 64*N) run the swap-AB expert GEMMs, whose token chunks are 64 rows:
-// their segments start on multiples of 64 rows instead.
+// T*k <= 64*N) run the swap-AB expert GEMMs, whose token chunks are 64 rows,
+// or 32 rows when an expert averages at most 16 (T*k <= 16*N): their segments
+// start on multiples of the chunk size instead.
 constexpr int kDecodeRowsPerExpert = 64;
+constexpr int kDecodeSmallRowsPerExpert = 16;
 
 // Kernel ids recorded next to a device error code in the status word.
 enum KernelId : int32_t {
@@ -223,8 +225,10 @@ cudaError_t launch_capacity(const Dims &D, const int32_t *topk_idx, const float 
 // Number of K slices of the decode-mode second GEMM (>= 1), or 0 when the
 // config is not decode-shaped (bf16 and T*k <= 64*N).
 int decode_splits(const Dims &D);
+// Token rows per chunk of the decode-mode expert FFN (32 or 64).
+int decode_chunk_rows(const Dims &D);
 // Segment alignment of the permuted buffers for this config.
-inline int row_align(const Dims &D) { return decode_splits(D) > 0 ? kDecodeRowsPerExpert : kRowAlign; }
+inline int row_align(const Dims &D) { return decode_splits(D) > 0 ? decode_chunk_rows(D) : kRowAlign; }
 
 // Swap-AB expert FFNs for decode-shaped batches, both GEMMs in one launch.
 // y_split holds the second GEMM's K slices 1..S-1 (S = decode_splits), each

@@ -86,9 +86,12 @@ def gpu_slots(g):
 
 
 def row_align(w):
-    """Segment alignment of the permuted buffers: 64 rows for decode-shaped
-    bf16 batches (T*k <= 64*N), else 128."""
-    return 64 if (w.dtype == "bf16" and w.T * w.k <= 64 * w.N) else 128
+    """Segment alignment of the permuted buffers: the decode chunk size for
+    decode-shaped bf16 batches (T*k <= 64*N: 64 rows, or 32 when
+    T*k <= 16*N), else 128."""
+    if w.dtype == "bf16" and w.T * w.k <= 64 * w.N:
+        return 32 if w.T * w.k <= 16 * w.N else 64
+    return 128
 
 
 def check_layout(g, k, align=128):

@@ -184,8 +184,11 @@ E2E_CASES = [
     custom(333, 64, 128, 8, 2, 1.25, router_bias="const:3:-60", seed=11),  # an expert nobody picks
     custom(256, 64, 256, 4, 1, 1.25, dtype="f32", router_bias="zipf", seed=12),  # fp32 with drops
 ] + [
-    # decode-shaped batches (bf16, T*k <= 64*N): swap-AB expert GEMMs, second GEMM split along d_ff
+    # decode-shaped batches (bf16, T*k <= 64*N): swap-AB expert GEMMs, second GEMM split along d_ff;
+    # 32-row token chunks while T*k <= 16*N, 64-row chunks above
     custom(64, 1024, 4096, 8, 2, math.inf, seed=13),
+    custom(64, 512, 1024, 8, 2, math.inf, router_bias="const:0:3", seed=17),  # expert 0 spans two 32-row chunks
+    custom(200, 512, 1024, 8, 2, math.inf, seed=18),  # 64-row chunks
     custom(48, 512, 2048, 8, 2, 1.0, router_bias="zipf", seed=14),  # drops
     custom(5, 768, 3072, 16, 4, math.inf, seed=15),  # fewer picks than experts
     custom(40, 520, 1000, 8, 2, 1.25, seed=16),  # ragged d and d_ff: partial k-blocks and weight tiles
