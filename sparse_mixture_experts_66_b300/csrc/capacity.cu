@@ -21,7 +21,7 @@
 //      used. Padding rows of the segment get token -1 and gate 0.
 #include <limits.h>
 
-#include "moe_internal.cuh"
+#include "tc_common.cuh"
 
 namespace moe {
 namespace {
@@ -300,7 +300,287 @@ __global__ void __launch_bounds__(kThreads) capacity_kernel(
   if (threadIdx.x == 0 && run_kept != kept_e) report_error(status, MOE_ERR_BOUNDS, kKCapAssign, 1000 + e);
 }
 
+// DSMEM helpers: a 32-bit / 4 x 32-bit load from a mapa'd shared address, and
+// the split cluster barrier (arrive with release, wait with acquire).
+__device__ __forceinline__ int ld_cluster(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ int4 ld_cluster_v4(uint32_t addr) {
+  int4 v;
+  asm volatile("ld.shared::cluster.v4.s32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// The same selection with the S CTAs of a cluster sharing one expert: CTA r
+// holds the requests [r*L, (r+1)*L) of the list in registers (L a multiple of
+// kItems, at most one pass of kThreads * kItems) and the CTAs add up what each
+// phase needs through distributed shared memory, in rank order:
+//   1. each CTA counts its slice for every expert; summed over the ranks, the
+//      counts give every CTA the same offsets;
+//   2. the radix passes add the ranks' 256 digit counts (integers: the sums,
+//      and so the C-th largest score, are exactly the single-CTA ones);
+//   3. each CTA counts its requests above the threshold and its ties; the ranks
+//      before r give how many ties precede the slice and how many rows the
+//      slice starts at, so slots and the tie quota follow token order across
+//      the whole list as in the single-CTA kernel.
+// Every remote read is followed by a cluster barrier before any CTA leaves.
+__global__ void __launch_bounds__(kThreads) capacity_cluster_kernel(
+    const int32_t *__restrict__ idx, const float *__restrict__ gate, const float *__restrict__ score, int64_t n,
+    int64_t L, int k, int N, int64_t C, int align, int32_t *counts_raw, int32_t *counts_kept, int32_t *offsets,
+    int32_t *row_of, int32_t *row_token, float *row_gate, int64_t R_max, int32_t *ffn_sync, int n_sync,
+    int32_t *status) {
+  pdl_wait();
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < n_sync; i += kThreads) ffn_sync[i] = 0;
+  extern __shared__ int s_hist[];  // [kWarps][N], then this slice's count per expert [N]
+  int *s_cnt = s_hist + kWarps * N;
+  __shared__ int s_warp[32];
+  __shared__ __align__(16) int s_sel[2][256];  // digit counts, alternate passes
+  __shared__ int s_x[2];                       // this slice: requests above the threshold, ties
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_need;
+  __shared__ int64_t s_off, s_end;
+  __shared__ int s_count;
+  const int S = (int)tc::cluster_size();
+  const int rank = (int)tc::cluster_rank();
+  const int e = blockIdx.x / S;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t lo = (int64_t)rank * L;
+  const int64_t hi = lo + L < n ? lo + L : n;
+  const int64_t i0 = lo + (int64_t)threadIdx.x * kItems;
+
+  Items it;
+  load_items(idx, score, gate, hi, i0, it);  // past the slice: expert -1
+
+  // 1. this slice's histogram, then the cluster's
+  for (int i = threadIdx.x; i < kWarps * N; i += kThreads) s_hist[i] = 0;
+  __syncthreads();
+#pragma unroll
+  for (int q = 0; q < kItems; ++q) {
+    const int ex = it.ie[q];
+    const unsigned peers = __match_any_sync(0xffffffffu, ex);
+    if (ex >= 0 && ex < N && lane == __ffs(peers) - 1) s_hist[warp * N + ex] += __popc(peers);
+  }
+  __syncthreads();
+  if (threadIdx.x < N) {
+    int c = 0;
+    for (int w = 0; w < kWarps; ++w) c += s_hist[w * N + threadIdx.x];
+    s_cnt[threadIdx.x] = c;
+  }
+  tc::cluster_sync_all();  // every slice's counts are visible to the cluster
+  int padded = 0, cnt = 0;
+  if (threadIdx.x < N) {
+    const uint32_t a = tc::saddr(s_cnt + threadIdx.x);
+    for (int q = 0; q < S; ++q) cnt += ld_cluster(tc::map_to_rank(a, (uint32_t)q));
+    padded = (int)round_up_rows(cnt < C ? cnt : C, align);
+  }
+  int total_rows;
+  const int excl = block_exclusive_scan(padded, s_warp, &total_rows);
+  if (threadIdx.x == e) {
+    s_off = excl;
+    s_end = (int64_t)excl + padded;
+    s_count = cnt;
+  }
+  __syncthreads();
+  const int64_t off = s_off;
+  const int count = s_count;
+  const int kept_e = (int64_t)count < C ? count : (int)C;
+  if (total_rows > R_max) {  // the whole cluster takes this branch (same totals)
+    // as the single-CTA kernel: an empty, well-formed dispatch
+    if (rank == 0 && threadIdx.x == 0) {
+      counts_raw[e] = count;
+      counts_kept[e] = 0;
+      offsets[e] = 0;
+      if (e == N - 1) offsets[N] = 0;
+      report_error(status, MOE_ERR_BOUNDS, kKCapAssign, e);
+    }
+#pragma unroll
+    for (int q = 0; q < kItems; ++q)
+      if (it.ie[q] == e) row_of[i0 + q] = -1;
+    tc::cluster_sync_all();  // no CTA leaves while a peer may read its counts
+    return;
+  }
+  if (rank == 0 && threadIdx.x == 0) {
+    counts_raw[e] = count;
+    counts_kept[e] = kept_e;
+    offsets[e] = (int32_t)off;
+    if (e == N - 1) offsets[N] = total_rows;
+  }
+
+  // 2. the C-th largest score of this expert, when it overflows (the same
+  // decision in every CTA of the cluster)
+  const bool overflow = (int64_t)count > C;
+  uint32_t thr = 0u;
+  int eq_keep = INT_MAX;
+  if (overflow) {
+    uint32_t prefix = 0u, mask = 0u;
+    int need = (int)C;
+    for (int shift = 24, p = 0; shift >= 0; shift -= 8, ++p) {
+      int *sel = s_sel[p & 1];
+      for (int i = threadIdx.x; i < 256; i += kThreads) sel[i] = 0;
+      __syncthreads();
+#pragma unroll
+      for (int q = 0; q < kItems; ++q)
+        if (it.ie[q] == e && (it.b[q] & mask) == prefix) atomicAdd(&sel[(it.b[q] >> shift) & 255u], 1);
+      // the ranks' counts are visible; the buffer is rewritten two passes on,
+      // after the next cluster barrier, which every rank reaches only once it
+      // has read this one
+      tc::cluster_sync_all();
+      if (warp == 0) {
+        int h[8] = {0, 0, 0, 0, 0, 0, 0, 0}, mine = 0;
+        const uint32_t a = tc::saddr(sel + lane * 8);
+        for (int q = 0; q < S; ++q) {
+          const uint32_t ra = tc::map_to_rank(a, (uint32_t)q);
+          const int4 u = ld_cluster_v4(ra), v = ld_cluster_v4(ra + 16u);
+          h[0] += u.x; h[1] += u.y; h[2] += u.z; h[3] += u.w;
+          h[4] += v.x; h[5] += v.y; h[6] += v.z; h[7] += v.w;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mine += h[j];
+        int suffix = mine;  // inclusive sum over lanes >= this one
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_down_sync(0xffffffffu, suffix, o);
+          if (lane + o < 32) suffix += v;
+        }
+        const int above = suffix - mine;
+        if (above < need && need <= suffix) {
+          int run = above, D = lane * 8;
+#pragma unroll
+          for (int j = 7; j >= 0; --j) {
+            if (run + h[j] >= need) {
+              D = lane * 8 + j;
+              break;
+            }
+            run += h[j];
+          }
+          s_prefix = prefix | ((uint32_t)D << shift);
+          s_need = need - run;
+        }
+      }
+      __syncthreads();
+      prefix = s_prefix;
+      need = s_need;
+      mask |= 255u << shift;
+      __syncthreads();
+    }
+    thr = prefix;
+    eq_keep = need;
+  }
+
+  // 3. slots in token order across the slices
+  int my_gt = 0, my_eq = 0;  // this thread: kept without question, ties at the threshold
+#pragma unroll
+  for (int q = 0; q < kItems; ++q) {
+    if (it.ie[q] != e) continue;
+    if (!overflow || it.b[q] > thr) ++my_gt;
+    else if (it.b[q] == thr) ++my_eq;
+  }
+  // both counts in one scan: each is at most kThreads * kItems < 2^16
+  int tot_pk;
+  const int ex_pk = block_exclusive_scan(my_gt | (my_eq << 16), s_warp, &tot_pk);
+  if (threadIdx.x == 0) {
+    s_x[0] = tot_pk & 0xffff;
+    s_x[1] = tot_pk >> 16;
+  }
+  tc::cluster_sync_all();
+  // ties and kept rows of the slices before this one
+  int eq_before = 0, kept_before = 0;
+  {
+    const uint32_t a = tc::saddr(s_x);
+    for (int q = 0; q < rank; ++q) {
+      const uint32_t ra = tc::map_to_rank(a, (uint32_t)q);
+      const int gt_q = ld_cluster(ra), eq_q = ld_cluster(ra + 4u);
+      int eq_kept = eq_keep - eq_before;
+      eq_kept = eq_kept < 0 ? 0 : (eq_kept > eq_q ? eq_q : eq_kept);
+      kept_before += gt_q + eq_kept;
+      eq_before += eq_q;
+    }
+  }
+  cluster_arrive();  // the last remote read: the peers may leave once all arrive
+  int eq_rank = eq_before + (ex_pk >> 16);
+  bool kept[kItems];
+  int my_kept = 0;
+#pragma unroll
+  for (int q = 0; q < kItems; ++q) {
+    bool kq = false;
+    if (it.ie[q] == e) {
+      if (!overflow || it.b[q] > thr) {
+        kq = true;
+      } else if (it.b[q] == thr) {
+        kq = eq_rank < eq_keep;
+        ++eq_rank;
+      }
+    }
+    kept[q] = kq;
+    my_kept += kq;
+  }
+  int tot_kept;
+  int slot = block_exclusive_scan(my_kept, s_warp, &tot_kept) + kept_before;
+  int64_t tq = i0 / k;
+  int rq = (int)(i0 - tq * k);
+  int32_t tok[kItems];
+#pragma unroll
+  for (int q = 0; q < kItems; ++q) {
+    tok[q] = (int32_t)tq;
+    if (++rq == k) {
+      rq = 0;
+      ++tq;
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < kItems; ++q) {
+    if (it.ie[q] != e) continue;
+    const int64_t i = i0 + q;
+    if (kept[q] && slot >= kept_e) {
+      report_error(status, MOE_ERR_BOUNDS, kKCapAssign, 2000 + e);
+      row_of[i] = -1;
+    } else if (kept[q]) {
+      const int64_t r = off + slot;
+      row_of[i] = (int32_t)r;
+      row_token[r] = tok[q];
+      row_gate[r] = it.g[q];
+      ++slot;
+    } else {
+      row_of[i] = -1;
+    }
+  }
+  if (rank == S - 1) {
+    for (int64_t r = off + kept_e + threadIdx.x; r < s_end; r += kThreads) {
+      row_token[r] = -1;
+      row_gate[r] = 0.f;
+    }
+    if (threadIdx.x == 0 && kept_before + tot_kept != kept_e)
+      report_error(status, MOE_ERR_BOUNDS, kKCapAssign, 1000 + e);
+  }
+  cluster_wait();
+}
+
 }  // namespace
+
+// CTAs per expert in the capacity launch: enough that every CTA holds its slice
+// of the request list in registers (at most 8, the portable cluster size), then
+// more while the launch stays one wave of CTAs and each slice keeps at least
+// 2048 requests. 1 selects the single-CTA kernel (which streams the list in
+// passes when it exceeds one CTA's registers).
+int capacity_cluster(const Dims &D) {
+  const int64_t n = D.T * D.k;
+  constexpr int64_t kChunk = (int64_t)kThreads * kItems;
+  int S = 1;
+  while (S < 8 && n > S * kChunk) S *= 2;
+  if (n > S * kChunk || (int64_t)D.N * S > num_sms()) return 1;
+  while (S < 8 && (int64_t)D.N * S * 2 <= num_sms() && n >= (int64_t)S * 2 * 2048) S *= 2;
+  return S;
+}
 
 cudaError_t launch_capacity(const Dims &D, const int32_t *topk_idx, const float *gate, const float *score,
                             int32_t *counts_raw, int32_t *counts_kept, int32_t *offsets, uint32_t *sel_thr,
@@ -311,6 +591,14 @@ cudaError_t launch_capacity(const Dims &D, const int32_t *topk_idx, const float 
   const int64_t n = D.T * D.k;
   const size_t smem = sizeof(int) * kWarps * D.N;
   const int n_sync = ffn_sync ? (int)ffn_sync_ints(D) : 0;
+  const int S = capacity_cluster(D);
+  if (S > 1) {
+    // slices of whole kItems groups (aligned vector loads), the last one short
+    const int64_t L = ((n + S - 1) / S + kItems - 1) / kItems * kItems;
+    return launch_k(capacity_cluster_kernel, dim3((unsigned)(D.N * S)), dim3(kThreads), smem + sizeof(int) * D.N, s,
+                    (unsigned)S, topk_idx, gate, score, n, L, D.k, D.N, D.C, row_align(D), counts_raw, counts_kept,
+                    offsets, row_of, row_token, row_gate, D.R_max, ffn_sync, n_sync, status);
+  }
   auto kern = n <= (int64_t)kThreads * kItems ? capacity_kernel<true> : capacity_kernel<false>;
   return launch_k(kern, dim3(D.N), dim3(kThreads), smem, s, 1u, topk_idx, gate, score, n, D.k, D.N, D.C,
                   row_align(D), counts_raw, counts_kept, offsets, row_of, row_token, row_gate, D.R_max, ffn_sync,

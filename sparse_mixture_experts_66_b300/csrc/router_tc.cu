@@ -16,11 +16,15 @@
 // shared memory), and after a cluster barrier rank 0 forms each logit as its
 // own partial plus ranks 1, 2, ... in that order: a fixed order, so the result
 // is deterministic. Splitting d lets a small batch stream x on S times as many
-// SMs. Rank 0's warps 2-5 then own one token each (TMEM lane = token): they
-// read the token's logits 32 columns at a time and do the softmax and the top-k
-// in registers (the k best kept by an unrolled insertion, ties to the lower
-// expert, picks in rank order). NP is N rounded up to 16..256; the W_g rows
-// past N are zero-filled by TMA and their columns are ignored.
+// SMs. Rank 0's epilogue warps then do the softmax and the top-k in
+// registers (TMEM lane = token; the k best kept by an unrolled insertion, ties
+// to the lower expert, picks in rank order). Up to 32 experts one thread owns a
+// token; from 64 on, 16 epilogue warps split each token's logits into four
+// column groups, exchange the group maxima, partial sums (added in group order)
+// and top-k candidates through shared memory, and group 0 merges the
+// candidates: the same picks as one pass over all columns. NP is N rounded up
+// to 16..256; the W_g rows past N are zero-filled by TMA and their columns are
+// ignored.
 #include <math.h>
 
 #include "tc_common.cuh"
@@ -32,9 +36,14 @@ using namespace tc;
 
 constexpr int kRM = 128;  // tokens per CTA (MMA M)
 constexpr int kRBK = 64;  // k-block: one 128-byte swizzle atom of bf16
-constexpr int kRThreads = 192;
-
 template <int NP, int S> struct RCfg {
+  // G column groups of epilogue warps: with many experts the per-token softmax
+  // and top-k would be a long serial chain in one thread, so 4 warps share each
+  // TMEM lane quadrant, a quarter of the logit columns each
+  static constexpr int G = NP >= 64 ? 4 : 1;
+  static constexpr int kCW = NP / G;  // logit columns per epilogue thread (a multiple of 16)
+  static constexpr int kEpiThreads = 128 * G;
+  static constexpr int kThreads = 64 + kEpiThreads;
   static constexpr int kXBytes = kRM * kRBK * 2;
   static constexpr int kWBytes = NP * kRBK * 2;
   static constexpr int kStageBytes = kXBytes + kWBytes;
@@ -48,12 +57,22 @@ template <int NP, int S> struct RCfg {
   static constexpr int kFit = (192 * 1024 - kPartBytes) / kStageBytes;
   static constexpr int kStages = kFit < 2 ? 2 : (kFit > 12 ? 12 : kFit);
   static constexpr int kTmemCols = NP < 32 ? 32 : NP;  // a power of two >= 32
+  // the column groups' exchange (per group and token: max, softmax partial sum,
+  // 8 top-k candidates as value and expert), in the stage ring, idle by then
+  static constexpr int kXchgBytes = G > 1 ? G * kRM * (4 + 4 + 8 * 8) : 0;
+  static_assert(kCW % 16 == 0, "column groups are whole 16-column TMEM loads");
+  static_assert(kXchgBytes <= kStages * kStageBytes, "exchange fits the stage ring");
 };
 
 // 16-byte store into another CTA's shared memory (a mapa'd address).
 __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
+}
+
+// Named barrier 1 over the epilogue warps only.
+template <int kCount> __device__ __forceinline__ void epi_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kCount) : "memory");
 }
 
 struct RCtrl {
@@ -69,7 +88,7 @@ template <int NP, int S> constexpr size_t router_smem() {
 }
 
 template <int NP, int S>
-__global__ void __launch_bounds__(kRThreads, 1)
+__global__ void __launch_bounds__(RCfg<NP, S>::kThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                      const float *__restrict__ router_bias, int64_t T_, int d, int N, int k,
                      int32_t *__restrict__ topk_idx, float *__restrict__ gate, float *__restrict__ score,
@@ -180,27 +199,34 @@ __global__ void __launch_bounds__(kRThreads, 1)
       }
     }
   } else {
-    const int q = warp & 3;
+    const int q = warp & 3;     // TMEM lane quadrant: tokens 32q..32q+31
+    const int g = (warp - 2) >> 2;  // column group: logit columns [g*CW, (g+1)*CW)
     const int row = q * 32 + lane;
+    const int cb = g * C::kCW;
     // the epilogue warps stage the logit bias (0 when none) while the MMAs run
-    for (int i = threadIdx.x - 64; i < NP; i += kRThreads - 64)
+    for (int i = threadIdx.x - 64; i < NP; i += C::kEpiThreads)
       c->bias[i] = (router_bias && i < N) ? router_bias[i] : 0.f;
-    asm volatile("bar.sync 1, %0;" ::"n"(kRThreads - 64) : "memory");  // the 4 epilogue warps only
+    epi_bar<C::kEpiThreads>();
     if (lane == 0) epi_ok = mbar_wait(&c->tfull, 0, abort, status, kKRouter, 30) ? 1 : 0;
     epi_ok = __shfl_sync(0xffffffffu, epi_ok, 0);
+    // one verdict for all epilogue warps: a warp whose wait ran out raised the
+    // abort flag before this barrier, so none of them joins the exchanges below
+    epi_bar<C::kEpiThreads>();
+    epi_ok = epi_ok && !*abort;
     if (S > 1 && rank != 0 && epi_ok) {
-      // ranks 1..S-1: this warp's 32 rows of partial logits into rank 0's slot
+      // ranks 1..S-1: this thread's columns of its row's partial logits into
+      // rank 0's slot
       tc_fence_after();
       const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
       const uint32_t dst = map_to_rank(saddr(part + ((int)(rank - 1) * kRM + row) * C::kPartStride), 0);
 #pragma unroll 1
-      for (int c0 = 0; c0 < NP; c0 += 32) {
-        uint32_t r[32];
+      for (int c0 = cb; c0 < cb + C::kCW; c0 += 16) {
+        uint32_t r[16];
         __syncwarp();
-        tmem_ld32(lane_base + (uint32_t)c0, r);
+        tmem_ld16(lane_base + (uint32_t)c0, r);
 #pragma unroll
-        for (int j = 0; j < 32; j += 4)
-          if (c0 + j < NP) st_cluster_v4(dst + (uint32_t)(c0 + j) * 4u, r[j], r[j + 1], r[j + 2], r[j + 3]);
+        for (int j = 0; j < 16; j += 4)
+          st_cluster_v4(dst + (uint32_t)(c0 + j) * 4u, r[j], r[j + 1], r[j + 2], r[j + 3]);
       }
     }
   }
@@ -208,116 +234,158 @@ __global__ void __launch_bounds__(kRThreads, 1)
 
   if (warp >= 2 && rank == 0 && epi_ok) {
     const int q = warp & 3;
+    const int g = (warp - 2) >> 2;
     const int row = q * 32 + lane;
+    const int cb = g * C::kCW;
     const int64_t t = t0 + row;
-    {
-      tc_fence_after();
-      const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-      float *mine = part + row * C::kPartStride;  // rank 1's slot, reused for the summed logits
-      if (S > 1) {
-        // logit = own partial + rank 1 + rank 2 + ..., in that order
+    tc_fence_after();
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    float *mine = part + row * C::kPartStride;  // rank 1's slot, reused for the summed logits
+    if (S > 1) {
+      // logit = own partial + rank 1 + rank 2 + ..., in that order
 #pragma unroll 1
-        for (int c0 = 0; c0 < NP; c0 += 32) {
-          uint32_t r[32];
-          __syncwarp();
-          tmem_ld32(lane_base + (uint32_t)c0, r);
+      for (int c0 = cb; c0 < cb + C::kCW; c0 += 16) {
+        uint32_t r[16];
+        __syncwarp();
+        tmem_ld16(lane_base + (uint32_t)c0, r);
 #pragma unroll
-          for (int j = 0; j < 32; j += 4) {
-            if (c0 + j >= NP) break;
-            float4 a = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
-                                   __uint_as_float(r[j + 3]));
+        for (int j = 0; j < 16; j += 4) {
+          float4 a = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
+                                 __uint_as_float(r[j + 3]));
 #pragma unroll
-            for (int src = 0; src < S - 1; ++src) {
-              const float4 p = *reinterpret_cast<const float4 *>(part + (src * kRM + row) * C::kPartStride + c0 + j);
-              a.x += p.x;
-              a.y += p.y;
-              a.z += p.z;
-              a.w += p.w;
-            }
-            *reinterpret_cast<float4 *>(mine + c0 + j) = a;
+          for (int src = 0; src < S - 1; ++src) {
+            const float4 p = *reinterpret_cast<const float4 *>(part + (src * kRM + row) * C::kPartStride + c0 + j);
+            a.x += p.x;
+            a.y += p.y;
+            a.z += p.z;
+            a.w += p.w;
+          }
+          *reinterpret_cast<float4 *>(mine + c0 + j) = a;
+        }
+      }
+    }
+    // 16 logits of this token from column c0 (without the bias)
+    auto load16 = [&](int c0, float(&v)[16]) {
+      if (S == 1) {
+        uint32_t r[16];
+        __syncwarp();  // the TMEM load is warp-collective
+        tmem_ld16(lane_base + (uint32_t)c0, r);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; j += 4) {
+          const float4 a = *reinterpret_cast<const float4 *>(mine + c0 + j);
+          v[j] = a.x;
+          v[j + 1] = a.y;
+          v[j + 2] = a.z;
+          v[j + 3] = a.w;
+        }
+      }
+    };
+    // the k best so far (value desc, expert asc): a candidate goes after an
+    // equal value, so ties keep the lower expert
+    float tv[8];
+    int te[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      tv[j] = -INFINITY;
+      te[j] = 0x7fffffff;
+    }
+    auto insert = [&](float v, int e) {
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        if (s < k && v > tv[s]) {
+          const float fv = tv[s];
+          const int fe = te[s];
+          tv[s] = v;
+          te[s] = e;
+          v = fv;
+          e = fe;
+        }
+      }
+    };
+    // pass 1: max and the k best of this thread's columns
+    float m = -INFINITY;
+#pragma unroll 1
+    for (int c0 = cb; c0 < cb + C::kCW; c0 += 16) {
+      float v16[16];
+      load16(c0, v16);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int e = c0 + j;
+        if (e >= N) break;  // padded expert columns
+        const float v = v16[j] + c->bias[e];
+        m = fmaxf(m, v);
+        insert(v, e);
+      }
+    }
+    // the groups' exchange (G > 1): group 0 of each token merges the others'
+    // candidates; every group needs the row max and the full denominator
+    float *xm = reinterpret_cast<float *>(base);  // [G][128] maxima
+    float *xs = xm + C::G * kRM;                  // [G][128] partial sums
+    float *xv = xs + C::G * kRM;                  // [G][8][128] candidate values
+    int *xe = reinterpret_cast<int *>(xv + C::G * 8 * kRM);  // [G][8][128] candidate experts
+    if (C::G > 1) {
+      // the ring was last written and read by the async proxy (TMA, MMA), all
+      // of it complete once the accumulator was
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      xm[g * kRM + row] = m;
+      if (g > 0)
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          if (s < k) {
+            xv[(g * 8 + s) * kRM + row] = tv[s];
+            xe[(g * 8 + s) * kRM + row] = te[s];
+          }
+      epi_bar<C::kEpiThreads>();
+      m = xm[row];
+#pragma unroll
+      for (int h = 1; h < C::G; ++h) m = fmaxf(m, xm[h * kRM + row]);
+    }
+    // pass 2: the softmax denominator, summed over groups in order
+    float sum = 0.f;
+#pragma unroll 1
+    for (int c0 = cb; c0 < cb + C::kCW; c0 += 16) {
+      float v16[16];
+      load16(c0, v16);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int e = c0 + j;
+        if (e >= N) break;
+        sum += expf(v16[j] + c->bias[e] - m);
+      }
+    }
+    if (C::G > 1) {
+      xs[g * kRM + row] = sum;
+      epi_bar<C::kEpiThreads>();
+      sum = 0.f;
+#pragma unroll
+      for (int h = 0; h < C::G; ++h) sum += xs[h * kRM + row];
+    }
+    if (probs) {  // router statistics: the full probability row and the logsumexp
+      // (the TMEM loads are warp-collective: every lane runs them, only lanes
+      // of real tokens store)
+#pragma unroll 1
+      for (int c0 = cb; c0 < cb + C::kCW; c0 += 16) {
+        float v16[16];
+        load16(c0, v16);
+        if (t < T_) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int e = c0 + j;
+            if (e >= N) break;
+            probs[t * N + e] = expf(v16[j] + c->bias[e] - m) / sum;
           }
         }
       }
-      // 32 logits of this token from column c0 (columns past NP read as 0)
-      auto load_chunk = [&](int c0, uint32_t(&r)[32]) {
-        if (S == 1) {
-          __syncwarp();  // the TMEM load is warp-collective
-          tmem_ld32(lane_base + (uint32_t)c0, r);
-        } else {
+      if (g == 0 && t < T_) lse[t] = m + logf(sum);
+    }
+    if (g == 0) {
+      for (int h = 1; h < C::G; ++h)
 #pragma unroll
-          for (int j = 0; j < 32; j += 4) {
-            const float4 v = c0 + j < NP ? *reinterpret_cast<const float4 *>(mine + c0 + j)
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
-            r[j] = __float_as_uint(v.x);
-            r[j + 1] = __float_as_uint(v.y);
-            r[j + 2] = __float_as_uint(v.z);
-            r[j + 3] = __float_as_uint(v.w);
-          }
-        }
-      };
-      // pass 1: max and the k best (value desc, expert asc)
-      float m = -INFINITY;
-      float tv[8];
-      int te[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        tv[j] = -INFINITY;
-        te[j] = 0x7fffffff;
-      }
-#pragma unroll 1
-      for (int c0 = 0; c0 < NP; c0 += 32) {
-        uint32_t r[32];
-        load_chunk(c0, r);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          int e = c0 + j;
-          if (e >= N) break;  // padded expert columns
-          float v = __uint_as_float(r[j]) + c->bias[e];
-          m = fmaxf(m, v);
-#pragma unroll
-          for (int s = 0; s < 8; ++s) {
-            if (s < k && v > tv[s]) {
-              const float fv = tv[s];
-              const int fe = te[s];
-              tv[s] = v;
-              te[s] = e;
-              v = fv;
-              e = fe;
-            }
-          }
-        }
-      }
-      // pass 2: the softmax denominator
-      float sum = 0.f;
-#pragma unroll 1
-      for (int c0 = 0; c0 < NP; c0 += 32) {
-        uint32_t r[32];
-        load_chunk(c0, r);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int e = c0 + j;
-          if (e >= N) break;
-          sum += expf(__uint_as_float(r[j]) + c->bias[e] - m);
-        }
-      }
-      if (probs) {  // router statistics: the full probability row and the logsumexp
-        // (the TMEM loads are warp-collective: every lane runs them, only
-        // lanes of real tokens store)
-#pragma unroll 1
-        for (int c0 = 0; c0 < NP; c0 += 32) {
-          uint32_t r[32];
-          load_chunk(c0, r);
-          if (t < T_) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int e = c0 + j;
-              if (e >= N) break;
-              probs[t * N + e] = expf(__uint_as_float(r[j]) + c->bias[e] - m) / sum;
-            }
-          }
-        }
-        if (t < T_) lse[t] = m + logf(sum);
-      }
+        for (int s = 0; s < 8; ++s)
+          if (s < k) insert(xv[(h * 8 + s) * kRM + row], xe[(h * 8 + s) * kRM + row]);
       if (t < T_) {
         float ex[8], sel = 0.f;
 #pragma unroll
@@ -364,7 +432,7 @@ cudaError_t launch_np(const Dims &D, const void *x, const void *w_g, const float
   const uint64_t dw[2] = {(uint64_t)D.d, (uint64_t)D.N};
   if (!make_map(&tx, x, 2, dx, kRM) || !make_map(&tw, w_g, 2, dw, NP)) return cudaErrorInvalidValue;
   const unsigned grid = (unsigned)((D.T + kRM - 1) / kRM) * S;
-  return launch_k(router_tc_kernel<NP, S>, dim3(grid), dim3(kRThreads), smem, s, (unsigned)S, tx, tw, router_bias,
+  return launch_k(router_tc_kernel<NP, S>, dim3(grid), dim3(RCfg<NP, S>::kThreads), smem, s, (unsigned)S, tx, tw, router_bias,
                   D.T, (int)D.d, D.N, D.k, topk_idx, gate, score, probs, lse, status);
 }
 

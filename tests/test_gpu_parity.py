@@ -34,16 +34,25 @@ STAGE_CASES = [
     custom(512, 64, 64, 256, 8, 1.0, seed=4),
     # every fp32 score of expert 0 rounds to 1.0: a full tie, resolved by token order
     custom(400, 128, 256, 8, 2, 1.0, router_bias="const:0:30", seed=9),
-    # more requests than one pass of the capacity CTA holds (8192): two chunks, compacted per expert, with overflow
+    # Above one CTA's registers (8192 requests) an expert's requests are split over a cluster of 2-8 CTAs,
+    # one slice each. 12000 requests: 4 slices of 3000, with overflow
     custom(6000, 64, 64, 8, 2, 1.0, router_bias="zipf", seed=17),
-    # 32000 requests: an expert's shared-memory list holds T = 16000 entries (a token's picks are distinct
-    # experts), and expert 0 receives nearly all tokens
+    # 32000 requests, 8 slices of 4000; expert 0 receives nearly all tokens
     custom(16000, 64, 64, 4, 2, 1.0, router_bias="const:0:6", seed=22),
-    # k = 1 with 17000 requests: the list holds every request (close to its largest size for N = 2)
+    # k = 1, 17000 requests: 8 slices of 2128 and a short last one (2104)
     custom(17000, 64, 64, 2, 1, 0.75, router_bias="const:1:3", seed=20),
-    # T = 20000 and 24000: more tokens than a list holds, the streaming form of the kernel runs
+    # 40000 and 48000 requests: 8 slices at 5000 and 6000
     custom(20000, 64, 64, 4, 2, 1.0, router_bias="const:0:6", seed=18),
     custom(24000, 64, 64, 4, 2, 1.0, router_bias="const:0:6", seed=19),
+    # a full tie across slices: expert 0's 7000 requests all score 1.0 and the quota (C = 4375) ends inside
+    # the third of four slices, so the ties and kept rows of the earlier slices decide the boundary
+    custom(7000, 64, 64, 8, 2, 2.5, router_bias="const:0:30", seed=23),
+    # the skewed batch's shape: 64 experts, 16384 requests in 2 slices, the head experts overflowing
+    custom(8192, 64, 64, 64, 2, 1.0, router_bias="zipf", seed=26),
+    # the single-CTA kernel streaming the list in passes: 66000 requests (more than 8 slices hold) and
+    # 64 experts x 4 slices (more CTAs than one wave)
+    custom(33000, 64, 64, 4, 2, 1.0, router_bias="const:0:6", seed=24),
+    custom(10000, 64, 64, 64, 2, 1.0, router_bias="zipf", seed=25),
 ]
 
 
@@ -151,6 +160,12 @@ ROUTER_CASES = [
     custom(1100, 512, 64, 32, 2, math.inf, seed=6),  # 32 experts, split of 4, ragged last tile
     custom(1100, 512, 64, 64, 4, math.inf, router_bias="zipf", seed=7),  # 64 experts, k=4, no split
     custom(2500, 384, 64, 16, 2, math.inf, seed=8),  # split of 2 (6 k-blocks)
+    # four column groups per token from 64 experts on: 40 experts leave group 2
+    # part-padded and group 3 empty; 128 and 200 experts give 32 and 64 columns
+    # per group (the top-k candidates of every group merged by group 0)
+    custom(1100, 512, 64, 40, 3, math.inf, router_bias="zipf", seed=9),
+    custom(1300, 256, 64, 128, 6, math.inf, seed=10),
+    custom(1500, 256, 64, 200, 8, math.inf, router_bias="zipf", seed=11),
 ]
 
 
@@ -164,6 +179,30 @@ def test_router_against_oracle(w):
     assert np.array_equal(g["topk_idx"][hi], ref["idx"][hi])
     assert np.allclose(g["gate"], ref["gate"], rtol=2e-5, atol=1e-6)
     assert np.allclose(g["gate"].sum(axis=1), 1.0, atol=1e-6)
+
+
+@pytest.mark.parametrize("N,k", [(64, 4), (256, 8)])
+def test_router_exact_ties_keep_the_lower_expert(N, k):
+    """Experts with identical W_g rows and bias have bit-identical logits; placed
+    in different column groups of the epilogue (every 16 or 64 experts) and
+    biased above the rest, they must be picked in ascending expert order, the
+    same order one pass over all columns gives."""
+    w = custom(1100, 128, 64, N, k, math.inf, seed=12)  # T > 1024: the tensor-core router
+    inp = draw(w)
+    step = N // 4
+    tied = [3 + step * j for j in range(4)]
+    wg = inp["w_g"].clone()
+    for e in tied[1:]:
+        wg[e] = wg[tied[0]]
+    bias = torch.zeros(N, dtype=torch.float32)
+    bias[tied] = 20.0
+    inp = dict(inp, w_g=wg, router_bias=bias)
+    g = parity.run_gpu(w, inp)
+    want = np.array(tied[: min(k, 4)])
+    assert (g["topk_idx"][:, : len(want)] == want).all()
+    if k > 4:  # the rest are ordinary picks, none of them tied experts
+        assert not np.isin(g["topk_idx"][:, 4:], tied).any()
+    assert np.allclose(g["gate"][:, : len(want)], g["gate"][:, :1], rtol=0, atol=0)
 
 
 # ---------------------------------------------------------------------------
@@ -277,6 +316,7 @@ def test_full_size_workloads(name):
 STATS_CASES = [
     custom(2048, 256, 64, 8, 2, 1.25, seed=21),  # bf16, tensor-core router
     custom(1500, 128, 64, 64, 2, 1.0, router_bias="zipf", seed=22),  # bf16, tensor-core router, N=64 + bias
+    custom(1100, 128, 64, 200, 4, 1.0, seed=26),  # bf16, tensor-core router, four 64-column groups, padded tail
     custom(300, 128, 64, 16, 4, math.inf, seed=23),  # bf16, split-column router
     custom(1200, 64, 64, 4, 1, 1.25, dtype="f32", seed=24),  # fp32, N <= 8 register router
     custom(1100, 64, 64, 40, 3, 1.0, dtype="f32", seed=25),  # fp32, generic router
