@@ -302,17 +302,18 @@ __global__ void __launch_bounds__(kThreads) capacity_kernel(
 
 // DSMEM helpers: a 32-bit / 4 x 32-bit load from a mapa'd shared address, and
 // the split cluster barrier (arrive with release, wait with acquire).
+// (no memory clobber: the cluster barrier before each read orders it, and the
+// loads of several ranks can then be in flight together)
 __device__ __forceinline__ int ld_cluster(uint32_t addr) {
   int v;
-  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
 __device__ __forceinline__ int4 ld_cluster_v4(uint32_t addr) {
   int4 v;
   asm volatile("ld.shared::cluster.v4.s32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr)
-               : "memory");
+               : "r"(addr));
   return v;
 }
 __device__ __forceinline__ void cluster_arrive() {
@@ -327,7 +328,10 @@ __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.w
 //   1. each CTA counts its slice for every expert; summed over the ranks, the
 //      counts give every CTA the same offsets;
 //   2. the radix passes add the ranks' 256 digit counts (integers: the sums,
-//      and so the C-th largest score, are exactly the single-CTA ones);
+//      and so the C-th largest score, are exactly the single-CTA ones); a pass
+//      whose chosen bin holds exactly the requests still to keep ends the
+//      search early: every request of that bin is kept, the same set a full
+//      search keeps;
 //   3. each CTA counts its requests above the threshold and its ties; the ranks
 //      before r give how many ties precede the slice and how many rows the
 //      slice starts at, so slots and the tie quota follow token order across
@@ -344,10 +348,10 @@ __global__ void __launch_bounds__(kThreads) capacity_cluster_kernel(
   extern __shared__ int s_hist[];  // [kWarps][N], then this slice's count per expert [N]
   int *s_cnt = s_hist + kWarps * N;
   __shared__ int s_warp[32];
-  __shared__ __align__(16) int s_sel[2][256];  // digit counts, alternate passes
-  __shared__ int s_x[2];                       // this slice: requests above the threshold, ties
-  __shared__ uint32_t s_prefix;
-  __shared__ int s_need;
+  __shared__ __align__(16) int s_sel[4][256];  // digit counts of each radix pass
+  __shared__ __align__(8) int s_x[2];          // this slice: requests above the threshold, ties
+  __shared__ uint32_t s_prefix[4];
+  __shared__ int s_need[4], s_last[4];
   __shared__ int64_t s_off, s_end;
   __shared__ int s_count;
   const int S = (int)tc::cluster_size();
@@ -363,6 +367,7 @@ __global__ void __launch_bounds__(kThreads) capacity_cluster_kernel(
 
   // 1. this slice's histogram, then the cluster's
   for (int i = threadIdx.x; i < kWarps * N; i += kThreads) s_hist[i] = 0;
+  for (int i = threadIdx.x; i < 4 * 256; i += kThreads) (&s_sel[0][0])[i] = 0;
   __syncthreads();
 #pragma unroll
   for (int q = 0; q < kItems; ++q) {
@@ -380,7 +385,11 @@ __global__ void __launch_bounds__(kThreads) capacity_cluster_kernel(
   int padded = 0, cnt = 0;
   if (threadIdx.x < N) {
     const uint32_t a = tc::saddr(s_cnt + threadIdx.x);
-    for (int q = 0; q < S; ++q) cnt += ld_cluster(tc::map_to_rank(a, (uint32_t)q));
+    int v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = q < S ? ld_cluster(tc::map_to_rank(a, (uint32_t)q)) : 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) cnt += v[q];
     padded = (int)round_up_rows(cnt < C ? cnt : C, align);
   }
   int total_rows;
@@ -419,30 +428,34 @@ __global__ void __launch_bounds__(kThreads) capacity_cluster_kernel(
   // 2. the C-th largest score of this expert, when it overflows (the same
   // decision in every CTA of the cluster)
   const bool overflow = (int64_t)count > C;
-  uint32_t thr = 0u;
+  uint32_t thr = 0u, thr_mask = ~0u;  // kept: (score bits & thr_mask) above thr, or equal within the quota
   int eq_keep = INT_MAX;
   if (overflow) {
     uint32_t prefix = 0u, mask = 0u;
     int need = (int)C;
     for (int shift = 24, p = 0; shift >= 0; shift -= 8, ++p) {
-      int *sel = s_sel[p & 1];
-      for (int i = threadIdx.x; i < 256; i += kThreads) sel[i] = 0;
-      __syncthreads();
+      int *sel = s_sel[p];  // zeroed in phase 1: no barrier before counting
 #pragma unroll
       for (int q = 0; q < kItems; ++q)
         if (it.ie[q] == e && (it.b[q] & mask) == prefix) atomicAdd(&sel[(it.b[q] >> shift) & 255u], 1);
-      // the ranks' counts are visible; the buffer is rewritten two passes on,
-      // after the next cluster barrier, which every rank reaches only once it
-      // has read this one
-      tc::cluster_sync_all();
+      tc::cluster_sync_all();  // the ranks' counts of this pass are visible
       if (warp == 0) {
         int h[8] = {0, 0, 0, 0, 0, 0, 0, 0}, mine = 0;
         const uint32_t a = tc::saddr(sel + lane * 8);
-        for (int q = 0; q < S; ++q) {
-          const uint32_t ra = tc::map_to_rank(a, (uint32_t)q);
-          const int4 u = ld_cluster_v4(ra), v = ld_cluster_v4(ra + 16u);
-          h[0] += u.x; h[1] += u.y; h[2] += u.z; h[3] += u.w;
-          h[4] += v.x; h[5] += v.y; h[6] += v.z; h[7] += v.w;
+        int4 u[8], w[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          u[q] = w[q] = make_int4(0, 0, 0, 0);
+          if (q < S) {
+            const uint32_t ra = tc::map_to_rank(a, (uint32_t)q);
+            u[q] = ld_cluster_v4(ra);
+            w[q] = ld_cluster_v4(ra + 16u);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          h[0] += u[q].x; h[1] += u[q].y; h[2] += u[q].z; h[3] += u[q].w;
+          h[4] += w[q].x; h[5] += w[q].y; h[6] += w[q].z; h[7] += w[q].w;
         }
 #pragma unroll
         for (int j = 0; j < 8; ++j) mine += h[j];
@@ -454,26 +467,29 @@ __global__ void __launch_bounds__(kThreads) capacity_cluster_kernel(
         }
         const int above = suffix - mine;
         if (above < need && need <= suffix) {
-          int run = above, D = lane * 8;
+          int run = above, D = lane * 8, hD = 0;
 #pragma unroll
           for (int j = 7; j >= 0; --j) {
             if (run + h[j] >= need) {
               D = lane * 8 + j;
+              hD = h[j];
               break;
             }
             run += h[j];
           }
-          s_prefix = prefix | ((uint32_t)D << shift);
-          s_need = need - run;
+          s_prefix[p] = prefix | ((uint32_t)D << shift);
+          s_need[p] = need - run;
+          s_last[p] = hD == need - run;  // the bin is kept whole
         }
       }
       __syncthreads();
-      prefix = s_prefix;
-      need = s_need;
+      prefix = s_prefix[p];
+      need = s_need[p];
       mask |= 255u << shift;
-      __syncthreads();
+      if (s_last[p]) break;
     }
     thr = prefix;
+    thr_mask = mask;
     eq_keep = need;
   }
 
@@ -482,8 +498,9 @@ __global__ void __launch_bounds__(kThreads) capacity_cluster_kernel(
 #pragma unroll
   for (int q = 0; q < kItems; ++q) {
     if (it.ie[q] != e) continue;
-    if (!overflow || it.b[q] > thr) ++my_gt;
-    else if (it.b[q] == thr) ++my_eq;
+    const uint32_t bm = it.b[q] & thr_mask;
+    if (!overflow || bm > thr) ++my_gt;
+    else if (bm == thr) ++my_eq;
   }
   // both counts in one scan: each is at most kThreads * kItems < 2^16
   int tot_pk;
@@ -497,13 +514,22 @@ __global__ void __launch_bounds__(kThreads) capacity_cluster_kernel(
   int eq_before = 0, kept_before = 0;
   {
     const uint32_t a = tc::saddr(s_x);
-    for (int q = 0; q < rank; ++q) {
-      const uint32_t ra = tc::map_to_rank(a, (uint32_t)q);
-      const int gt_q = ld_cluster(ra), eq_q = ld_cluster(ra + 4u);
+    int gt_q[8], eq_q[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {  // all loads in flight together
+      gt_q[q] = eq_q[q] = 0;
+      if (q < rank) {
+        const uint32_t ra = tc::map_to_rank(a, (uint32_t)q);
+        gt_q[q] = ld_cluster(ra);
+        eq_q[q] = ld_cluster(ra + 4u);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
       int eq_kept = eq_keep - eq_before;
-      eq_kept = eq_kept < 0 ? 0 : (eq_kept > eq_q ? eq_q : eq_kept);
-      kept_before += gt_q + eq_kept;
-      eq_before += eq_q;
+      eq_kept = eq_kept < 0 ? 0 : (eq_kept > eq_q[q] ? eq_q[q] : eq_kept);
+      kept_before += gt_q[q] + eq_kept;
+      eq_before += eq_q[q];
     }
   }
   cluster_arrive();  // the last remote read: the peers may leave once all arrive
@@ -514,9 +540,10 @@ __global__ void __launch_bounds__(kThreads) capacity_cluster_kernel(
   for (int q = 0; q < kItems; ++q) {
     bool kq = false;
     if (it.ie[q] == e) {
-      if (!overflow || it.b[q] > thr) {
+      const uint32_t bm = it.b[q] & thr_mask;
+      if (!overflow || bm > thr) {
         kq = true;
-      } else if (it.b[q] == thr) {
+      } else if (bm == thr) {
         kq = eq_rank < eq_keep;
         ++eq_rank;
       }
@@ -526,8 +553,8 @@ __global__ void __launch_bounds__(kThreads) capacity_cluster_kernel(
   }
   int tot_kept;
   int slot = block_exclusive_scan(my_kept, s_warp, &tot_kept) + kept_before;
-  int64_t tq = i0 / k;
-  int rq = (int)(i0 - tq * k);
+  int tq = (int)i0 / k;  // at most 8 slices of 8192 requests: 32-bit division
+  int rq = (int)i0 - tq * k;
   int32_t tok[kItems];
 #pragma unroll
   for (int q = 0; q < kItems; ++q) {

@@ -87,7 +87,9 @@ template <int NP, int S> constexpr size_t router_smem() {
   return 1024 + (size_t)C::kStages * C::kStageBytes + (size_t)C::kPartBytes + sizeof(RCtrl);
 }
 
-template <int NP, int S>
+// KM: the top-k insertion's depth, k rounded up to 2 or 8 (each logit costs
+// KM compare-and-swap steps, the epilogue's main work with many experts)
+template <int NP, int S, int KM>
 __global__ void __launch_bounds__(RCfg<NP, S>::kThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                      const float *__restrict__ router_bias, int64_t T_, int d, int N, int k,
@@ -294,7 +296,7 @@ __global__ void __launch_bounds__(RCfg<NP, S>::kThreads, 1)
     }
     auto insert = [&](float v, int e) {
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {
+      for (int s = 0; s < KM; ++s) {
         if (s < k && v > tv[s]) {
           const float fv = tv[s];
           const int fe = te[s];
@@ -333,7 +335,7 @@ __global__ void __launch_bounds__(RCfg<NP, S>::kThreads, 1)
       xm[g * kRM + row] = m;
       if (g > 0)
 #pragma unroll
-        for (int s = 0; s < 8; ++s)
+        for (int s = 0; s < KM; ++s)
           if (s < k) {
             xv[(g * 8 + s) * kRM + row] = tv[s];
             xe[(g * 8 + s) * kRM + row] = te[s];
@@ -384,7 +386,7 @@ __global__ void __launch_bounds__(RCfg<NP, S>::kThreads, 1)
     if (g == 0) {
       for (int h = 1; h < C::G; ++h)
 #pragma unroll
-        for (int s = 0; s < 8; ++s)
+        for (int s = 0; s < KM; ++s)
           if (s < k) insert(xv[(h * 8 + s) * kRM + row], xe[(h * 8 + s) * kRM + row]);
       if (t < T_) {
         float ex[8], sel = 0.f;
@@ -414,8 +416,8 @@ __global__ void __launch_bounds__(RCfg<NP, S>::kThreads, 1)
   }
 }
 
-template <int NP, int S>
-cudaError_t launch_np(const Dims &D, const void *x, const void *w_g, const float *router_bias, int32_t *topk_idx,
+template <int NP, int S, int KM>
+cudaError_t launch_npk(const Dims &D, const void *x, const void *w_g, const float *router_bias, int32_t *topk_idx,
                       float *gate, float *score, float *probs, float *lse, int32_t *status, cudaStream_t s) {
   static PerDevice<int> attr;  // this instance's shared-memory size, set once per device
   const size_t smem = router_smem<NP, S>();
@@ -423,7 +425,8 @@ cudaError_t launch_np(const Dims &D, const void *x, const void *w_g, const float
   const cudaError_t ae = attr.get(
       [smem](int *v) {
         *v = 1;
-        return cudaFuncSetAttribute(router_tc_kernel<NP, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        return cudaFuncSetAttribute(router_tc_kernel<NP, S, KM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem);
       },
       &set);
   if (ae != cudaSuccess) return ae;
@@ -432,8 +435,15 @@ cudaError_t launch_np(const Dims &D, const void *x, const void *w_g, const float
   const uint64_t dw[2] = {(uint64_t)D.d, (uint64_t)D.N};
   if (!make_map(&tx, x, 2, dx, kRM) || !make_map(&tw, w_g, 2, dw, NP)) return cudaErrorInvalidValue;
   const unsigned grid = (unsigned)((D.T + kRM - 1) / kRM) * S;
-  return launch_k(router_tc_kernel<NP, S>, dim3(grid), dim3(RCfg<NP, S>::kThreads), smem, s, (unsigned)S, tx, tw, router_bias,
+  return launch_k(router_tc_kernel<NP, S, KM>, dim3(grid), dim3(RCfg<NP, S>::kThreads), smem, s, (unsigned)S, tx, tw, router_bias,
                   D.T, (int)D.d, D.N, D.k, topk_idx, gate, score, probs, lse, status);
+}
+
+template <int NP, int S>
+cudaError_t launch_np(const Dims &D, const void *x, const void *w_g, const float *router_bias, int32_t *topk_idx,
+                      float *gate, float *score, float *probs, float *lse, int32_t *status, cudaStream_t s) {
+  if (D.k <= 2) return launch_npk<NP, S, 2>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
+  return launch_npk<NP, S, 8>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
 }
 
 // CTAs per 128-token tile: split d over a cluster of 4 or 2 while the tiles
