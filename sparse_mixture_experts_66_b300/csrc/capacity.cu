@@ -335,7 +335,9 @@ __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.w
 //   3. each CTA counts its requests above the threshold and its ties; the ranks
 //      before r give how many ties precede the slice and how many rows the
 //      slice starts at, so slots and the tie quota follow token order across
-//      the whole list as in the single-CTA kernel.
+//      the whole list as in the single-CTA kernel. An expert that does not
+//      overflow keeps every request: its slice starts after the expert's
+//      requests in the earlier slices, known from step 1, and no exchange runs.
 // Every remote read is followed by a cluster barrier before any CTA leaves.
 __global__ void __launch_bounds__(kThreads) capacity_cluster_kernel(
     const int32_t *__restrict__ idx, const float *__restrict__ gate, const float *__restrict__ score, int64_t n,
@@ -353,7 +355,7 @@ __global__ void __launch_bounds__(kThreads) capacity_cluster_kernel(
   __shared__ uint32_t s_prefix[4];
   __shared__ int s_need[4], s_last[4];
   __shared__ int64_t s_off, s_end;
-  __shared__ int s_count;
+  __shared__ int s_count, s_before;
   const int S = (int)tc::cluster_size();
   const int rank = (int)tc::cluster_rank();
   const int e = blockIdx.x / S;
@@ -382,22 +384,30 @@ __global__ void __launch_bounds__(kThreads) capacity_cluster_kernel(
     s_cnt[threadIdx.x] = c;
   }
   tc::cluster_sync_all();  // every slice's counts are visible to the cluster
-  int padded = 0, cnt = 0;
+  int padded = 0, cnt = 0, before = 0;
   if (threadIdx.x < N) {
     const uint32_t a = tc::saddr(s_cnt + threadIdx.x);
     int v[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) v[q] = q < S ? ld_cluster(tc::map_to_rank(a, (uint32_t)q)) : 0;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) cnt += v[q];
+    for (int q = 0; q < 8; ++q) {
+      before += q < rank ? v[q] : 0;
+      cnt += v[q];
+    }
     padded = (int)round_up_rows(cnt < C ? cnt : C, align);
   }
+  // the counts were the last remote read unless the expert overflows: the
+  // peers may leave once every CTA has arrived (the wait comes at the end, or
+  // before the radix passes)
+  cluster_arrive();
   int total_rows;
   const int excl = block_exclusive_scan(padded, s_warp, &total_rows);
   if (threadIdx.x == e) {
     s_off = excl;
     s_end = (int64_t)excl + padded;
     s_count = cnt;
+    s_before = before;  // the expert's requests in the slices before this one
   }
   __syncthreads();
   const int64_t off = s_off;
@@ -415,7 +425,7 @@ __global__ void __launch_bounds__(kThreads) capacity_cluster_kernel(
 #pragma unroll
     for (int q = 0; q < kItems; ++q)
       if (it.ie[q] == e) row_of[i0 + q] = -1;
-    tc::cluster_sync_all();  // no CTA leaves while a peer may read its counts
+    cluster_wait();  // no CTA leaves while a peer may read its counts
     return;
   }
   if (rank == 0 && threadIdx.x == 0) {
@@ -431,6 +441,7 @@ __global__ void __launch_bounds__(kThreads) capacity_cluster_kernel(
   uint32_t thr = 0u, thr_mask = ~0u;  // kept: (score bits & thr_mask) above thr, or equal within the quota
   int eq_keep = INT_MAX;
   if (overflow) {
+    cluster_wait();  // (completes the arrival after the counts)
     uint32_t prefix = 0u, mask = 0u;
     int need = (int)C;
     for (int shift = 24, p = 0; shift >= 0; shift -= 8, ++p) {
@@ -494,25 +505,25 @@ __global__ void __launch_bounds__(kThreads) capacity_cluster_kernel(
   }
 
   // 3. slots in token order across the slices
-  int my_gt = 0, my_eq = 0;  // this thread: kept without question, ties at the threshold
+  int eq_before = 0, kept_before = 0, eq_rank = 0;
+  if (overflow) {
+    int my_gt = 0, my_eq = 0;  // this thread: kept without question, ties at the threshold
 #pragma unroll
-  for (int q = 0; q < kItems; ++q) {
-    if (it.ie[q] != e) continue;
-    const uint32_t bm = it.b[q] & thr_mask;
-    if (!overflow || bm > thr) ++my_gt;
-    else if (bm == thr) ++my_eq;
-  }
-  // both counts in one scan: each is at most kThreads * kItems < 2^16
-  int tot_pk;
-  const int ex_pk = block_exclusive_scan(my_gt | (my_eq << 16), s_warp, &tot_pk);
-  if (threadIdx.x == 0) {
-    s_x[0] = tot_pk & 0xffff;
-    s_x[1] = tot_pk >> 16;
-  }
-  tc::cluster_sync_all();
-  // ties and kept rows of the slices before this one
-  int eq_before = 0, kept_before = 0;
-  {
+    for (int q = 0; q < kItems; ++q) {
+      if (it.ie[q] != e) continue;
+      const uint32_t bm = it.b[q] & thr_mask;
+      if (bm > thr) ++my_gt;
+      else if (bm == thr) ++my_eq;
+    }
+    // both counts in one scan: each is at most kThreads * kItems < 2^16
+    int tot_pk;
+    const int ex_pk = block_exclusive_scan(my_gt | (my_eq << 16), s_warp, &tot_pk);
+    if (threadIdx.x == 0) {
+      s_x[0] = tot_pk & 0xffff;
+      s_x[1] = tot_pk >> 16;
+    }
+    tc::cluster_sync_all();
+    // ties and kept rows of the slices before this one
     const uint32_t a = tc::saddr(s_x);
     int gt_q[8], eq_q[8];
 #pragma unroll
@@ -531,9 +542,11 @@ __global__ void __launch_bounds__(kThreads) capacity_cluster_kernel(
       kept_before += gt_q[q] + eq_kept;
       eq_before += eq_q[q];
     }
+    cluster_arrive();  // the last remote read: the peers may leave once all arrive
+    eq_rank = eq_before + (ex_pk >> 16);
+  } else {
+    kept_before = s_before;  // every request of the expert is kept
   }
-  cluster_arrive();  // the last remote read: the peers may leave once all arrive
-  int eq_rank = eq_before + (ex_pk >> 16);
   bool kept[kItems];
   int my_kept = 0;
 #pragma unroll

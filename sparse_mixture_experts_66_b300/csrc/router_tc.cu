@@ -448,12 +448,12 @@ cudaError_t launch_np(const Dims &D, const void *x, const void *w_g, const float
 
 // CTAs per 128-token tile: split d over a cluster of 4 or 2 while the tiles
 // alone would leave most SMs idle and every rank keeps at least two k-blocks.
-// Only for NP <= 32: with more experts the per-token softmax and top-k, which
-// rank 0 alone runs, dominate the router and a split measured slower overall.
+// Up to 64 experts: beyond, the per-token softmax and top-k, which rank 0
+// alone runs, outweigh the faster stream of x.
 int router_splits(const Dims &D, int NP) {
   const int64_t tiles = (D.T + kRM - 1) / kRM;
   const int kb = (int)((D.d + kRBK - 1) / kRBK);
-  if (NP > 32) return 1;
+  if (NP > 64) return 1;
   for (int S = 4; S >= 2; S >>= 1)
     if (tiles * S <= num_sms() && kb >= 2 * S) return S;
   return 1;
@@ -477,7 +477,7 @@ cudaError_t launch_router_tc(const Dims &D, const void *x, const void *w_g, cons
   if (D.dt != MOE_DT_BF16 || D.N > 256) return cudaErrorNotSupported;
   if (D.N <= 16) return launch_split<16>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
   if (D.N <= 32) return launch_split<32>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
-  if (D.N <= 64) return launch_np<64, 1>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
+  if (D.N <= 64) return launch_split<64>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
   if (D.N <= 128) return launch_np<128, 1>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
   return launch_np<256, 1>(D, x, w_g, router_bias, topk_idx, gate, score, probs, lse, status, s);
 }
