@@ -261,6 +261,9 @@ def test_deterministic_across_runs():
 
 @pytest.mark.parametrize("w", [
     custom(700, 256, 512, 8, 2, 1.0, router_bias="zipf", seed=15),
+    # larger batches: 6000 rows (d = 1024) with drops and a zipf skew, 20000 rows over 16 experts
+    custom(3000, 1024, 512, 8, 2, 1.0, router_bias="zipf", seed=27),
+    custom(10000, 512, 256, 16, 2, 1.25, seed=28),
     # decode-shaped: the swap-AB expert FFN and the K-sliced combine
     custom(64, 1024, 4096, 8, 2, math.inf, seed=23),
 ], ids=lambda w: w.name)
