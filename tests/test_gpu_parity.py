@@ -496,3 +496,21 @@ def test_expert_ffn_accepts_16_byte_aligned_outputs():
     rows = int(g["offsets"][-1])
     assert torch.equal(h16[:rows], v["h"][:rows])
     assert torch.equal(y16[:rows], v["y_perm"][:rows])
+
+
+@pytest.mark.skipif(torch.cuda.is_available() and torch.cuda.device_count() < 2, reason="needs a second GPU")
+def test_forward_on_a_second_device():
+    """The one-time set-up of the tensor-core kernels (shared-memory opt-ins,
+    SM and resident-pair counts) is kept per device: a forward on device 1
+    after one on device 0 launches and gives the same bits."""
+    w = custom(1100, 256, 512, 8, 2, 1.25, seed=29)
+    inp = draw(w)
+    outs = []
+    for dev in (0, 1):
+        with torch.cuda.device(dev):
+            d = {k: (None if v is None else v.to(f"cuda:{dev}")) for k, v in inp.items()}
+            cfg = moe.config_of(w)
+            y, ws = moe.forward(cfg, d["x"], d["w_g"], d["w1"], d["b1"], d["w2"], d["b2"], d["router_bias"])
+            ws.status()
+            outs.append(y.cpu())
+    assert torch.equal(outs[0], outs[1])
