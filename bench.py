@@ -255,6 +255,18 @@ def algorithmic(w, counts_kept):
                 bytes_ffn_weights=bytes_ffn_weights)
 
 
+def timing_events(n, per, stream):
+    """n lists of `per` timing events, each recorded once and synchronised
+    here: torch creates a CUDA event at its first record, and hundreds of
+    creations inside a timed loop can make it host-bound."""
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(per)] for _ in range(n)]
+    for row in evs:
+        for e in row:
+            e.record(stream)
+    stream.synchronize()
+    return evs
+
+
 def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
@@ -307,7 +319,7 @@ def run_ours(args, world, rank, local):
     # Timed region 1 (the value): events at the step boundaries only, around
     # each replay, so the launches inside a step overlap through programmatic
     # dependent launch as they do for a user.
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    ev = timing_events(K, 2, stream)
     clocks = ClockSampler(local)
     clocks.start()
     barrier(world)
@@ -330,7 +342,7 @@ def run_ours(args, world, rank, local):
     # Timed region 2 (the roofline): the same K steps with events around the
     # expert FFN launch, the dominant kernel (events there stop its launch
     # from overlapping its neighbours, so this region does not give the value).
-    ev_f = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    ev_f = timing_events(K, 2, stream)
     for i in range(K):
         if use_flush:
             flush()
@@ -347,7 +359,7 @@ def run_ours(args, world, rank, local):
     # Stage breakdown (reported, not timed for the value): an event after every
     # stage call, which serialises the stages.
     K2 = min(K, 20)
-    ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K2)]
+    ev2 = timing_events(K2, 5, stream)
     for i in range(K2):
         if use_flush:
             flush()
@@ -389,7 +401,7 @@ def run_ours(args, world, rank, local):
     barrier(world)
     if use_flush:
         e2e_mode = "serial: copy in, forward, copy out per step; L2 flushed between steps outside the events"
-        e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        e2e_ev = timing_events(K, 2, stream)
         for i in range(K):
             flush()
             e2e_ev[i][0].record(stream)
@@ -411,6 +423,12 @@ def run_ours(args, world, rank, local):
             fwd_done = [ev() for _ in range(n)]
             out_done = [ev() for _ in range(n)]
             t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            # torch creates a CUDA event at its first record: do that here, not
+            # inside the timed steps (hundreds of creations made the first timed
+            # run host-bound)
+            for e in in_done + fwd_done + out_done + [t0, t1]:
+                e.record(stream)
+            torch.cuda.synchronize(device)
             t0.record(stream)
             s_in.wait_event(t0)
             s_out.wait_event(t0)
@@ -434,9 +452,11 @@ def run_ours(args, world, rank, local):
             torch.cuda.synchronize(device)
             return t0.elapsed_time(t1) / n
 
-        # untimed warm-up of the same pattern on the same streams and buffers
-        # (the first pipelined steps pay one-time costs of the copy streams)
-        pipelined(max(args.warmup, 3))
+        # untimed warm-up: the same pattern, as many steps as the timed run, on
+        # the same streams and buffers (torch's pinned-memory allocator records
+        # an event per asynchronous copy and grows its event pool during the
+        # first long run)
+        pipelined(K)
         barrier(world)
         e2e_ms = pipelined(K)
     barrier(world)
