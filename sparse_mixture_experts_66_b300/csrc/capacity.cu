@@ -7,12 +7,17 @@
 // requests fill the expert's buffer in token order (the pseudocode's
 // expert_buffer), which fixes each request's slot.
 //
-// One launch, one CTA per expert, no atomics deciding any output:
+// One launch, no atomics deciding any output. Lists under 4096 requests: one
+// CTA per expert with the list in registers. Up to 65 536 requests: a cluster
+// of 2-8 CTAs per expert, each holding a slice in registers
+// (capacity_cluster_kernel below: the same steps, the slices' counts added in
+// rank order). Longer lists, or clusters that would not fit one wave of CTAs:
+// one CTA per expert streaming the list in passes. The single-CTA form:
 //   1. every CTA counts the requests of all N experts (warp-aggregated with
 //      match_any into per-warp rows of a shared histogram), so each CTA can
 //      compute every segment offset itself: offset[e] = sum over e' < e of
-//      roundup(min(count[e'], C), A), A = 128 rows (64 for decode-shaped
-//      batches). No CTA waits for another;
+//      roundup(min(count[e'], C), A), A = 128 rows (the decode chunk, 32 or 64
+//      rows, for decode-shaped batches). No CTA waits for another;
 //   2. if its expert overflows, the CTA radix-selects (4 passes of 8 bits over
 //      the fp32 score's bit pattern, which orders non-negative floats) the C-th
 //      largest score and how many requests equal to it are still kept;
