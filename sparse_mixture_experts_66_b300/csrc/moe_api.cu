@@ -81,6 +81,7 @@ Dims shared_dims(const Dims &D) {
   Dims S1 = D;
   S1.N = 1;
   S1.k = 1;
+  S1.C = D.T;  // the one expert takes every token
   S1.R_max = (D.T + kRowAlign - 1) / kRowAlign * kRowAlign;
   return S1;
 }
