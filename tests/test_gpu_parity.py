@@ -131,7 +131,8 @@ def test_expert_ffn_rows_against_oracle(w):
     assert max(errs) <= parity.TOL[w.dtype] * max(scale)
 
 
-@pytest.mark.parametrize("w", [STAGE_CASES[0], WORKLOADS[HEADLINE]], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [STAGE_CASES[0], WORKLOADS[HEADLINE], custom(1024, 520, 712, 16, 2, 1.0, seed=51)],
+                         ids=lambda w: w.name)
 def test_hidden_activations_within_bf16_rounding_of_exact_gelu(w):
     """h = GELU(x_perm W1^T + b1) from the first GEMM's epilogue equals the
     exact (erf) GELU of the oracle up to the bf16 rounding of h and the fp32
@@ -232,6 +233,10 @@ E2E_CASES = [
     custom(5, 768, 3072, 16, 4, math.inf, seed=15),  # fewer picks than experts
     custom(40, 520, 1000, 8, 2, 1.25, seed=16),  # ragged d and d_ff: partial k-blocks and weight tiles
     custom(700, 136, 200, 4, 2, 1.25, seed=50),  # CTA-pair path, d_ff = 8 mod 16: 16-byte h stores
+    # the narrow CTA-pair form (C <= 256: 128-column tiles): every expert a masked 128-row tail, with ragged d
+    # and d_ff (partial k-block, partial n-tiles); then full 256-row blocks mixed with tails
+    custom(1024, 520, 712, 16, 2, 1.0, seed=51),
+    custom(3000, 256, 640, 32, 2, 1.25, router_bias="zipf", seed=52),
 ]
 
 
