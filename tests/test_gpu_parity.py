@@ -47,6 +47,11 @@ STAGE_CASES = [
     # a full tie across slices: expert 0's 7000 requests all score 1.0 and the quota (C = 4375) ends inside
     # the third of four slices, so the ties and kept rows of the earlier slices decide the boundary
     custom(7000, 64, 64, 8, 2, 2.5, router_bias="const:0:30", seed=23),
+    # eight slices of a fully tied expert: 32000 requests (L = 4000) and a quota C = 12000 that ends exactly at a
+    # slice boundary (tokens 0..11999 are requests 0..23999); k = 1 with 30000 requests (L = 3752, a short last
+    # slice) and a quota of 13500 that ends inside the fourth slice
+    custom(16000, 64, 64, 4, 2, 1.5, router_bias="const:0:30", seed=29),
+    custom(30000, 64, 64, 2, 1, 0.9, router_bias="const:0:30", seed=30),
     # the skewed batch's shape: 64 experts, 16384 requests in 2 slices, the head experts overflowing
     custom(8192, 64, 64, 64, 2, 1.0, router_bias="zipf", seed=26),
     # the single-CTA kernel streaming the list in passes: 66000 requests (more than 8 slices hold) and
