@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(RCfg<NP, S>::kThreads, 1)
     epi_bar<C::kEpiThreads>();
     if (lane == 0) epi_ok = mbar_wait(&c->tfull, 0, abort, status, kKRouter, 30) ? 1 : 0;
     epi_ok = __shfl_sync(0xffffffffu, epi_ok, 0);
-    // one verdict for all epilogue warps: a warp whose wait ran out raised the
+    // one outcome for all epilogue warps: a warp whose wait ran out raised the
     // abort flag before this barrier, so none of them joins the exchanges below
     epi_bar<C::kEpiThreads>();
     epi_ok = epi_ok && !*abort;
