@@ -610,8 +610,6 @@ __global__ void __launch_bounds__(kThreads) capacity_cluster_kernel(
   cluster_wait();
 }
 
-}  // namespace
-
 // CTAs per expert in the capacity launch: enough that every CTA holds its slice
 // of the request list in registers (at most 8, the portable cluster size), then
 // more while the launch stays one wave of CTAs and each slice keeps at least
@@ -626,6 +624,8 @@ int capacity_cluster(const Dims &D) {
   while (S < 8 && (int64_t)D.N * S * 2 <= num_sms() && n >= (int64_t)S * 2 * 2048) S *= 2;
   return S;
 }
+
+}  // namespace
 
 cudaError_t launch_capacity(const Dims &D, const int32_t *topk_idx, const float *gate, const float *score,
                             int32_t *counts_raw, int32_t *counts_kept, int32_t *offsets, uint32_t *sel_thr,
