@@ -330,6 +330,9 @@ STATS_CASES = [
     custom(2048, 256, 64, 8, 2, 1.25, seed=21),  # bf16, tensor-core router
     custom(1500, 128, 64, 64, 2, 1.0, router_bias="zipf", seed=22),  # bf16, tensor-core router, N=64 + bias
     custom(1100, 128, 64, 200, 4, 1.0, seed=26),  # bf16, tensor-core router, four 64-column groups, padded tail
+    # 64 experts with d split over clusters of 4 (8 k-blocks) and four column groups: the summed partials feed
+    # the stored probability rows
+    custom(1500, 512, 64, 64, 2, 1.0, router_bias="zipf", seed=31),
     custom(300, 128, 64, 16, 4, math.inf, seed=23),  # bf16, split-column router
     custom(1200, 64, 64, 4, 1, 1.25, dtype="f32", seed=24),  # fp32, N <= 8 register router
     custom(1100, 64, 64, 40, 3, 1.0, dtype="f32", seed=25),  # fp32, generic router
@@ -449,6 +452,8 @@ EC_CASES = [
     custom(800, 128, 256, 16, 2, 1.0, router_bias="zipf", seed=42),  # N = 16 > 8: the many-pick combine
     custom(40, 512, 1024, 8, 2, 1.0, seed=43),  # T <= 64: decode-shaped (swap-AB) FFN
     custom(256, 64, 256, 4, 1, 1.25, dtype="f32", seed=44),  # fp32 SIMT path
+    # 64 experts on the tensor-core router (d split over clusters of 4, four column groups per token)
+    custom(1100, 512, 256, 64, 2, 1.0, seed=45),
 ]
 
 
