@@ -169,6 +169,7 @@ ROUTER_CASES = [
     # four column groups per token from 64 experts on: 40 experts leave group 2
     # part-padded and group 3 empty; 128 and 200 experts give 32 and 64 columns
     # per group (the top-k candidates of every group merged by group 0)
+    custom(1100, 256, 64, 16, 4, math.inf, seed=53),  # k = 4 on the one-thread-per-token epilogue (8-step insertion)
     custom(1100, 512, 64, 40, 3, math.inf, router_bias="zipf", seed=9),
     custom(1300, 256, 64, 128, 6, math.inf, seed=10),
     custom(1500, 256, 64, 200, 8, math.inf, router_bias="zipf", seed=11),
